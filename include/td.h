@@ -1,0 +1,186 @@
+/*
+ * td.h -- C ABI of the TwoTower block-diffusion denoise step (sm_103a).
+ *
+ * Sources. The method is described only in prose, on these pages:
+ *   [chathome]  "NVIDIA、Nemotron-Labs-TwoTowerを公開：凍結された自己回帰バックボーン上に
+ *               構築されたオープンウェイト拡散言語モデル" (news.chathome.org).
+ *               Paragraphs used: the inference paragraph ("推論では…": per-layer KV cache,
+ *               bidirectional in-block attention, layer-aligned cross-attention, adaLN-single),
+ *               the generation paragraph ("生成はブロックごとに…": blocks of S [MASK], T steps,
+ *               commit) and the evaluation paragraph ("2×H100 GPUでのBF16評価では…":
+ *               confidence masking, threshold gamma = 0.8, block size S = 16).
+ *   [aiboss]    "Nemotron-Labs-TwoTower - NVIDIAのオープンソースデュアルタワーアーキテクチャ
+ *               普及言語モデル" (aiboss88.com), section "技術原理" (technical principle).
+ *   [aikraft]   "Архитектурный прорыв: разделение задач" (aikraft.ru), benchmark paragraph
+ *               (gamma = 0.8, S = 16, BF16).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller unless it is documented
+ *     as a host pointer. The library never allocates device memory: scratch space is the
+ *     caller's `ws` buffer of at least td_workspace_size() bytes, 256-byte aligned.
+ *   - bf16 tensors are IEEE bfloat16 stored as uint16; fp32 tensors are IEEE binary32.
+ *     All tensors are dense row-major (C order) with the shapes given below; weights are
+ *     stored [out_features, in_features] (each output column's weights contiguous).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call is
+ *     asynchronous on it, except td_decode_block, which reads one flag back per step.
+ *   - Arguments are validated on the host before anything is launched; a rejected call
+ *     launches nothing and returns TD_ERR_INVALID_ARG / TD_ERR_UNSUPPORTED /
+ *     TD_ERR_WORKSPACE. No C++ exception crosses this boundary.
+ *   - Device-side waits are bounded. A kernel whose wait runs out records a code in a
+ *     device error word and returns early; td_device_error() reads (and clears) it.
+ *   - Shapes supported by the kernels: D in {64, 128}; Hq % Hkv == 0; 1 <= S <= 64;
+ *     d % 64 == 0; V % 8 == 0; B*S <= 65536; Lmax >= 0.
+ */
+#ifndef TD_H_
+#define TD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum td_status {
+  TD_OK = 0,
+  TD_ERR_INVALID_ARG = 1,   /* null pointer, negative/zero size, bad gamma/t/T          */
+  TD_ERR_WORKSPACE = 2,     /* ws == NULL or ws_bytes < td_workspace_size(), misaligned */
+  TD_ERR_UNSUPPORTED = 3,   /* a shape outside the limits listed above                  */
+  TD_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch error, ...)           */
+  TD_ERR_NOT_CONVERGED = 5, /* td_decode_block: positions still [MASK] after step T     */
+  TD_ERR_DEVICE_TIMEOUT = 6 /* a kernel's bounded wait ran out (see td_device_error)    */
+} td_status;
+
+/* Problem sizes (the pages' notation): B sequences, S block size, d hidden size,
+ * Hq query heads, Hkv KV heads (GQA: query head h uses KV head h / (Hq/Hkv)),
+ * D head dim, V vocabulary (the [MASK] token id is V, one past the LM-head range),
+ * Lmax context KV capacity per sequence, n_layers stacked denoiser attention layers. */
+typedef struct td_dims {
+  int B, S, d, Hq, Hkv, D, V, Lmax, n_layers;
+} td_dims;
+
+/* One denoiser attention layer and the context tower's KV cache of the same layer
+ * ([chathome] inference paragraph: each denoiser layer cross-attends to the matching
+ * context-tower layer).
+ *   wqkv  bf16 [(Hq + 2*Hkv)*D, d]  rows 0..Hq*D-1 = W_q^T, then W_k^T, then W_v^T
+ *   wo    bf16 [d, Hq*D]            W_o^T
+ *   ada_E fp32 [6, d]               per-layer adaLN-single table E_l (rows: shift, scale,
+ *                                   gate, then three rows of the out-of-scope MLP sublayer)
+ *   k_ctx bf16 [B, Hkv, Lmax, D]    context keys of this layer (prompt + committed tokens)
+ *   v_ctx bf16 [B, Hkv, Lmax, D]    context values of this layer */
+typedef struct td_layer {
+  const void* wqkv;
+  const void* wo;
+  const float* ada_E;
+  const void* k_ctx;
+  const void* v_ctx;
+} td_layer;
+
+/* Selector for td_workspace_size(). */
+enum {
+  TD_FN_ADALN_MODULATE = 0,
+  TD_FN_BLOCK_ATTENTION = 1,
+  TD_FN_LMHEAD_COMMIT = 2,
+  TD_FN_DENOISE_STEP = 3,
+  TD_FN_DECODE_BLOCK = 4
+};
+
+/* Bytes of caller-provided scratch that entry point `fn` needs for `dims`; 0 if none,
+ * (size_t)-1 if dims are invalid or unsupported. */
+size_t td_workspace_size(const td_dims* dims, int fn);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* td_status_string(td_status s);
+
+/* adaLN-single modulation ([chathome] inference paragraph: the diffusion timestep
+ * modulates every layer through adaLN-single).
+ *   m = E + phi (fp32 [6, d] each); for each row r of h:
+ *   x_hat = (h_r - mean(h_r)) / sqrt(var(h_r) + eps)   (population variance, no affine)
+ *   x_mod_r = bf16(x_hat * (1 + m[1]) + m[0])
+ * h: bf16 [rows, d] (read only). x_mod: bf16 [rows, d] (written). No workspace.
+ * Errors: TD_ERR_INVALID_ARG (null, rows <= 0, d <= 0, eps < 0), TD_ERR_UNSUPPORTED
+ * (d % 8 != 0). */
+td_status td_adaln_modulate(const void* h, const float* E, const float* phi, int rows, int d,
+                            float eps, void* x_mod, void* stream);
+
+/* Fused block attention ([chathome] inference paragraph: bidirectional attention inside
+ * the block, causal to past clean blocks, layer-aligned cross-attention to the context
+ * tower's per-layer KV cache). For every sequence b, block position i, query head h,
+ * with g = h / (Hq/Hkv) and L_b = ctx_len ? ctx_len[b] : Lmax:
+ *   keys   = k_ctx[b, g, 0:L_b, :] followed by k_blk[b, 0:S, g, :]
+ *   values = v_ctx[b, g, 0:L_b, :] followed by v_blk[b, 0:S, g, :]
+ *   o[b, i, h, :] = bf16( sum_j softmax_j(q[b,i,h,:] . keys_j / sqrt(D)) values_j )
+ * one softmax over the union (no mask: the cache holds only past tokens).
+ *   q      bf16 [B, S, Hq, D]       k_blk, v_blk bf16 [B, S, Hkv, D]
+ *   k_ctx, v_ctx bf16 [B, Hkv, Lmax, D]
+ *   ctx_len int32 [B] or NULL (0 <= ctx_len[b] <= Lmax)
+ *   o      bf16 [B, S, Hq, D] (written)
+ *   lse    fp32 [B, S, Hq] or NULL: natural log of sum_j exp(q . keys_j / sqrt(D))
+ *   ws     >= td_workspace_size(dims, TD_FN_BLOCK_ATTENTION) bytes.
+ * Only B, S, Hq, Hkv, D, Lmax of dims are read. */
+td_status td_block_attention(const td_dims* dims, const void* q, const void* k_blk,
+                             const void* v_blk, const void* k_ctx, const void* v_ctx,
+                             const int* ctx_len, void* o, float* lse, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/* LM head + confidence-masking commit ([chathome] generation and evaluation paragraphs:
+ * tokens of the block commit when their confidence clears gamma; several commit per step).
+ * For every row r = b*S + i:  z = h_r . W_lm^T (fp32 accumulate, never stored),
+ *   conf[r] = max_v softmax(z)_v = 1 / sum_v exp(z_v - max z),
+ *   pred[r] = the lowest v with z_v = max z.
+ * Commit, per sequence b: C = { i : masked[b,i] && conf >= gamma }; if C is empty and some
+ * position is masked, C = { the lowest-index masked i of maximal conf }; if force_all,
+ * C = every masked i. For i in C: tokens[b,i] = pred, masked[b,i] = 0.
+ * n_committed[b] = |C|; *all_done = 1 if no position of any sequence is still masked.
+ *   h     bf16 [B*S, d]           w_lm bf16 [V, d]
+ *   tokens int32 [B, S] in/out    masked uint8 [B, S] in/out (1 = still [MASK])
+ *   conf  fp32 [B, S] out (every row)   pred int32 [B, S] out (every row)
+ *   n_committed int32 [B] out           all_done int32 [1] out
+ * Only B, S, d, V of dims are read. Committed positions are never rewritten. */
+td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm, float gamma,
+                           int force_all, int* tokens, unsigned char* masked, float* conf,
+                           int* pred, int* n_committed, int* all_done, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* One denoising step of the denoiser tower over the block ([chathome] inference and
+ * generation paragraphs). If h is NULL the block's input is embedded from the tokens:
+ *   h0[b, i] = bf16(emb[tokens[b, i]] + pos[i])   (emb bf16 [V+1, d], row V = [MASK];
+ *   pos bf16 [S, d] stands in for the position information of the out-of-scope layers)
+ * else h (bf16 [B*S, d], read only) is the input. Then for each layer l:
+ *   m = E_l + phi_t; x_mod = adaLN(h) as in td_adaln_modulate (eps = 1e-6);
+ *   [q | k | v] = bf16(x_mod . wqkv^T); o = td_block_attention(...);
+ *   h = bf16(h + m[2] * (o . wo^T))            (m[2] is the gate)
+ * and finally td_lmhead_commit with force_all = (t == T).
+ *   phi_t fp32 [6, d]: the shared adaLN-single timestep vector of step t (1 <= t <= T).
+ *   layers: HOST array of dims->n_layers td_layer structs (device pointers inside).
+ *   ctx_len int32 [B] device or NULL.  Other outputs as in td_lmhead_commit. */
+td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int* ctx_len,
+                          const void* h, const void* emb, const void* pos, const void* w_lm,
+                          const float* phi_t, int t, int T, float gamma, int* tokens,
+                          unsigned char* masked, float* conf, int* pred, int* n_committed,
+                          int* all_done, void* ws, size_t ws_bytes, void* stream);
+
+/* Block decode loop ([chathome] generation paragraph: a block starts as S [MASK] tokens,
+ * is refined for T steps and committed). Runs td_denoise_step (embedding path) for
+ * t = t_start .. T with phi_t = phi_table[t-1] (fp32 [T, 6, d]) and stops after the first
+ * step that leaves no position masked. tokens/masked hold the block state on entry
+ * (all [MASK] for a fresh block; a partially committed state resumes a stopped loop).
+ * steps_taken: HOST int, set to the number of steps run. Reads all_done back once per step.
+ * Returns TD_ERR_NOT_CONVERGED only if positions remain masked after step T (cannot
+ * happen with force-commit at t == T; kept for callers that stop early). */
+td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
+                          const void* emb, const void* pos, const void* w_lm,
+                          const float* phi_table, int t_start, int T, float gamma, int* tokens,
+                          unsigned char* masked, float* conf, int* pred, int* n_committed,
+                          int* all_done, int* steps_taken, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* Reads and clears the device error word that bounded waits write (0 = none); the
+ * current device is used. Synchronises the device. Returns TD_ERR_CUDA if the read fails. */
+td_status td_device_error(int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TD_H_ */
