@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark of the TwoTower block-diffusion denoise path on one B300 (or N replicas).
+
+Workload (the full block decode): B=64 sequences, context KV length 8192 per sequence, block
+S=16, T=16 steps, 6 stacked denoiser attention layers each with its own context-layer KV
+cache, d=4096, 32 query / 2 KV heads, head_dim 128, vocabulary 131072, gamma=0.8, bf16.
+One bench step = one td_decode_block call on a fresh all-[MASK] block: embedding, adaLN,
+QKV projection, fused block attention, gated O projection, LM head + commit, repeated until
+every position is committed. Inputs are seeded synthetic tensors created in HBM.
+
+value = committed tokens / s (B*S per block / block wall time), whole job over all ranks.
+Also printed: denoised tokens / s (B*S*steps / time), the roofline of the dominant kernel,
+the fp64 oracle timed on the host cores on a bounded sample, end-to-end numbers through the
+Python API with host buffers, and SM clocks sampled during the timed region.
+
+Multi-GPU: the path shards by sequence and needs no exchange, so N ranks run N independent
+replicas (weak scaling); only a barrier and a max of the elapsed time cross ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+WORKLOAD = dict(workload="block decode loop", B=64, S=16, L=8192, n_layers=6, d=4096, Hq=32,
+                Hkv=2, D=128, V=131072, T=16, gamma=0.8)
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0)
+
+
+def peaks():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------------------------ distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ oracle sample
+
+class OracleSampler:
+    """The fp64 oracle decoding blocks of a few sequences of the workload, step by step
+    (a bounded sample: it continues the same block across calls, starting a new block when
+    one is fully committed)."""
+
+    def __init__(self, wl, rows=(0,)):
+        import numpy as np
+        self.np = np
+        self.wl = wl
+        self.rows = list(rows)
+        self.layers = [{k: (v[self.rows].cpu() if k in ("k_ctx", "v_ctx") else v.cpu())
+                        for k, v in L.items()} for L in wl.layers]
+        self.w, self.emb = wl.w_lm.cpu(), wl.emb.cpu()
+        self.pos, self.phi = wl.pos.cpu(), wl.phi_table.cpu()
+        self.d = dict(wl.dims.as_dict(), B=len(self.rows))
+        self._reset()
+
+    def _reset(self):
+        dm = self.wl.dims
+        self.tok = self.np.full((len(self.rows), dm.S), dm.V)
+        self.msk = self.np.ones((len(self.rows), dm.S), bool)
+        self.t = 1
+
+    def step(self) -> int:
+        import oracle
+        wl = self.wl
+        r = oracle.denoise_step(self.d, self.layers, self.phi[self.t - 1], self.w, self.tok,
+                                self.msk, wl.gamma, self.t, wl.T, emb=self.emb, pos=self.pos)
+        self.tok, self.msk = r["tokens"], r["masked"]
+        self.t += 1
+        if not self.msk.any() or self.t > wl.T:
+            self._reset()
+        return int(r["n_committed"].sum())
+
+    def describe(self, steps: int) -> str:
+        dm = self.wl.dims
+        return (f"fp64 oracle on {len(self.rows)} of {dm.B} sequences: {steps} denoise steps "
+                f"of the block loop ({dm.n_layers} layers, L={dm.Lmax}, V={dm.V}); "
+                f"committed tokens / wall time")
+
+
+def oracle_sample(wl, seconds_budget: float, max_steps: int):
+    s = OracleSampler(wl)
+    committed = steps = 0
+    t0 = time.perf_counter()
+    while steps < max_steps:
+        committed += s.step()
+        steps += 1
+        if time.perf_counter() - t0 > seconds_budget:
+            break
+    el = time.perf_counter() - t0
+    return committed / el, torch.get_num_threads(), s.describe(steps), steps
+
+
+# ------------------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world, rank, local = dist_setup()
+    from block_diffusion_lm_denoise_b300 import synth
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import block_diffusion_lm_denoise_b300 as td
+    td.lib()   # fails loudly if the CUDA library is missing
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.decode_loop(dev, seed=4 + rank)
+    dm = wl.dims
+    dims = dm.as_dict()
+    M = dm.B * dm.S
+    ws = td.workspace(dims, td.TD_FN_DECODE_BLOCK, dev)
+    tokens = torch.empty_like(wl.tokens)
+    masked = torch.empty_like(wl.masked)
+    outs = td._outs(dm.B, dm.S, dev, None, None, None, None)
+
+    def one_block():
+        tokens.fill_(dm.V)
+        masked.fill_(1)
+        return td.td_decode_block(dims, wl.layers, wl.emb, wl.pos, wl.w_lm, wl.phi_table, wl.T,
+                                  wl.gamma, tokens, masked, conf=outs[0], pred=outs[1],
+                                  n_committed=outs[2], all_done=outs[3], ws=ws)
+
+    for _ in range(max(3, args.warmup)):
+        one_block()
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps_taken = []
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            steps_taken.append(one_block())
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world)
+    total_steps = sum(steps_taken)
+    value = world * M * args.steps / (ms_max / 1e3)
+    denoised = world * M * total_steps / (ms_max / 1e3)
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    tok_h = torch.full((dm.B, dm.S), dm.V, dtype=torch.int32).pin_memory()
+    msk_h = torch.ones((dm.B, dm.S), dtype=torch.uint8).pin_memory()
+    tok_out = torch.empty((dm.B, dm.S), dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = time.perf_counter()
+    for _ in range(args.steps):
+        tokens.copy_(tok_h, non_blocking=True)
+        masked.copy_(msk_h, non_blocking=True)
+        td.td_decode_block(dims, wl.layers, wl.emb, wl.pos, wl.w_lm, wl.phi_table, wl.T,
+                           wl.gamma, tokens, masked, conf=outs[0], pred=outs[1],
+                           n_committed=outs[2], all_done=outs[3], ws=ws)
+        tok_out.copy_(tokens, non_blocking=True)
+        torch.cuda.synchronize()
+    e_s = max_over_ranks(time.perf_counter() - e0, world)
+    e2e = world * M * args.steps / e_s
+
+    # ---------------------------------------------------------------- roofline (isolated kernels)
+    pk, pk_kind = peaks()
+    reps = 10
+    lay = wl.layers[0]
+    q = synth.normal((dm.B, dm.S, dm.Hq, dm.D), 1.0, 99, "bench.q", dev)
+    kb = synth.normal((dm.B, dm.S, dm.Hkv, dm.D), 1.0, 99, "bench.kb", dev)
+    vb = synth.normal((dm.B, dm.S, dm.Hkv, dm.D), 1.0, 99, "bench.vb", dev)
+    o = torch.empty_like(q)
+    aws = td.workspace(dims, td.TD_FN_BLOCK_ATTENTION, dev)
+    for _ in range(3):
+        td.td_block_attention(dims, q, kb, vb, lay["k_ctx"], lay["v_ctx"], o=o, ws=aws)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(reps):
+        td.td_block_attention(dims, q, kb, vb, lay["k_ctx"], lay["v_ctx"], o=o, ws=aws)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    attn_ms = a0.elapsed_time(a1) / reps
+    kv_bytes = 2 * dm.B * dm.Hkv * dm.Lmax * dm.D * 2
+    attn_bytes = kv_bytes + (q.numel() + o.numel() + kb.numel() + vb.numel()) * 2
+    attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9
+
+    h = synth.normal((M, dm.d), 1.0, 99, "bench.h", dev)
+    lws = td.workspace(dims, td.TD_FN_LMHEAD_COMMIT, dev)
+    tk = torch.empty_like(tokens)
+    mk = torch.empty_like(masked)
+    for _ in range(3):
+        tk.fill_(dm.V); mk.fill_(1)
+        td.td_lmhead_commit(dims, h, wl.w_lm, wl.gamma, False, tk, mk, *outs, ws=lws)
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for _ in range(reps):
+        td.td_lmhead_commit(dims, h, wl.w_lm, wl.gamma, False, tk, mk, *outs, ws=lws)
+    l1.record(stream)
+    torch.cuda.synchronize()
+    lm_ms = l0.elapsed_time(l1) / reps
+    lm_flops = 2.0 * M * dm.d * dm.V
+    lm_tflops = lm_flops / (lm_ms / 1e3) / 1e12
+    step_ms = ms / max(1, total_steps)
+    attn_share = dm.n_layers * attn_ms / step_ms
+    lm_share = lm_ms / step_ms
+    roof_attn = {"kernel": "attn_fused_kernel<128> (+merge)", "bound": "hbm",
+                 "achieved": round(attn_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                 "frac": round(attn_gbs / pk["hbm_gbs"], 4), "traffic": None,
+                 "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(attn_ms, 4),
+                 "share_of_step": round(attn_share, 3), "peak_source": pk_kind}
+    roof_lm = {"kernel": "gemm_tn_kernel<256,4,LMHEAD> + merge_commit", "bound": "tensor",
+               "achieved": round(lm_tflops, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+               "frac": round(lm_tflops / pk["bf16_tflops"], 4), "traffic": None,
+               "algorithmic_flops_per_launch": lm_flops, "ms_per_launch": round(lm_ms, 4),
+               "share_of_step": round(lm_share, 3), "peak_source": pk_kind}
+    dominant, other = (roof_attn, roof_lm) if attn_share >= lm_share else (roof_lm, roof_attn)
+
+    launches_per_step = 1 + dm.n_layers * 4 + 2   # embed, 6 x (adaLN, QKV, attention, O-proj), LM, commit
+    result = {
+        "metric": "committed tokens/sec (block decode, S=16, gamma=0.8)",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights and context KV of the stated shapes)",
+        "config": dict(WORKLOAD, parallelism=f"replicas x{world}",
+                       l2="inputs larger than L2 (3.2 GB of context KV + 1 GB LM head per step)"),
+        "denoised_tokens_per_s": round(denoised, 1),
+        "denoise_steps_per_block": round(total_steps / args.steps, 3),
+        "gpu_launches": launches_per_step * total_steps,
+        "clocks": clocks.summary(),
+        "roofline": dominant,
+        "roofline_other": other,
+        "e2e": {"value": round(e2e, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": tok_h.numel() * 4 + msk_h.numel(),
+                "d2h_bytes_per_step": tok_out.numel() * 4},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_sample(wl, args.cpu_budget, 64)
+        result["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cores,
+                                  "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, world, rank):
+    """The fp64 oracle on the host cores, same workload, metric and unit; rank 0 only.
+    Each bench step is one oracle denoise step of one sequence's block (bounded sample)."""
+    if rank != 0:
+        return
+    from block_diffusion_lm_denoise_b300 import synth
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    wl = synth.decode_loop(dev, seed=4)
+    smp = OracleSampler(wl)
+    for _ in range(args.warmup):
+        smp.step()
+    committed = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        committed += smp.step()
+    el = time.perf_counter() - t0
+    value = committed / el
+    result = {
+        "impl": "reference",
+        "metric": "committed tokens/sec (block decode, S=16, gamma=0.8)",
+        "value": round(value, 4),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": dict(WORKLOAD, parallelism="host cores"),
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s",
+                         "cores": torch.get_num_threads(), "kind": "oracle",
+                         "sample": smp.describe(args.steps)},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

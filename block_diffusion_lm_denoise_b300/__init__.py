@@ -1,0 +1,231 @@
+"""Python binding of the TwoTower block-diffusion denoise-step library (libtdenoise.so).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels behind the C ABI
+declared in include/td.h. PyTorch supplies device memory and streams. There is no CPU
+fallback: if the library is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtdenoise.so")
+
+TD_FN_ADALN_MODULATE = 0
+TD_FN_BLOCK_ATTENTION = 1
+TD_FN_LMHEAD_COMMIT = 2
+TD_FN_DENOISE_STEP = 3
+TD_FN_DECODE_BLOCK = 4
+
+# Every symbol the header declares (checked by the tests).
+EXPORTED = ("td_workspace_size", "td_status_string", "td_adaln_modulate", "td_block_attention",
+            "td_lmhead_commit", "td_denoise_step", "td_decode_block", "td_device_error")
+
+
+class TdError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {text} ({status})")
+        self.status = status
+
+
+class td_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("B", "S", "d", "Hq", "Hkv", "D", "V", "Lmax",
+                                             "n_layers")]
+
+
+class td_layer(ctypes.Structure):
+    _fields_ = [("wqkv", ctypes.c_void_p), ("wo", ctypes.c_void_p), ("ada_E", ctypes.c_void_p),
+                ("k_ctx", ctypes.c_void_p), ("v_ctx", ctypes.c_void_p)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m block_diffusion_lm_denoise_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.td_workspace_size.argtypes = [ctypes.POINTER(td_dims), i]
+        L.td_workspace_size.restype = sz
+        L.td_status_string.argtypes = [i]
+        L.td_status_string.restype = ctypes.c_char_p
+        L.td_adaln_modulate.argtypes = [vp, vp, vp, i, i, f, vp, vp]
+        L.td_block_attention.argtypes = [ctypes.POINTER(td_dims), vp, vp, vp, vp, vp, vp, vp, vp,
+                                         vp, sz, vp]
+        L.td_lmhead_commit.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, vp, vp, vp, vp, vp,
+                                       vp, vp, sz, vp]
+        L.td_denoise_step.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer), vp, vp,
+                                      vp, vp, vp, vp, i, i, f, vp, vp, vp, vp, vp, vp, vp, sz,
+                                      vp]
+        L.td_decode_block.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer), vp, vp,
+                                      vp, vp, vp, i, i, f, vp, vp, vp, vp, vp, vp,
+                                      ctypes.POINTER(i), vp, sz, vp]
+        L.td_device_error.argtypes = [ctypes.POINTER(i)]
+        for name in EXPORTED:
+            if name not in ("td_workspace_size", "td_status_string"):
+                getattr(L, name).restype = i
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise TdError(fn, status, lib().td_status_string(status).decode())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_dims(B, S, d, Hq, Hkv, D, V, Lmax, n_layers) -> td_dims:
+    return td_dims(B, S, d, Hq, Hkv, D, V, Lmax, n_layers)
+
+
+def dims_from(obj) -> td_dims:
+    """td_dims from a mapping or an object with the nine fields."""
+    get = (lambda k: obj[k]) if isinstance(obj, dict) else (lambda k: getattr(obj, k))
+    return td_dims(*(int(get(k)) for k in ("B", "S", "d", "Hq", "Hkv", "D", "V", "Lmax",
+                                          "n_layers")))
+
+
+def td_workspace_size(dims, fn: int) -> int:
+    dm = dims if isinstance(dims, td_dims) else dims_from(dims)
+    n = lib().td_workspace_size(ctypes.byref(dm), fn)
+    if n == ctypes.c_size_t(-1).value:
+        raise TdError("td_workspace_size", 3, "unsupported or invalid dims")
+    return int(n)
+
+
+def workspace(dims, fn: int, device="cuda") -> torch.Tensor:
+    """A device byte buffer of td_workspace_size(dims, fn) bytes (at least 256)."""
+    return torch.empty(max(256, td_workspace_size(dims, fn)), dtype=torch.uint8, device=device)
+
+
+def td_device_error() -> int:
+    code = ctypes.c_int(0)
+    _check("td_device_error", lib().td_device_error(ctypes.byref(code)))
+    return code.value
+
+
+def td_adaln_modulate(h: torch.Tensor, E: torch.Tensor, phi: torch.Tensor, eps: float = 1e-6,
+                      x_mod: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    rows, d = h.shape
+    if x_mod is None:
+        x_mod = torch.empty_like(h)
+    _check("td_adaln_modulate",
+           lib().td_adaln_modulate(_ptr(h), _ptr(E), _ptr(phi), rows, d, eps, _ptr(x_mod),
+                                   _stream(stream)))
+    return x_mod
+
+
+def td_block_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len=None, o=None, lse=None,
+                       ws=None, stream=None):
+    dm = dims if isinstance(dims, td_dims) else dims_from(dims)
+    if o is None:
+        o = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(dm, TD_FN_BLOCK_ATTENTION, q.device)
+    _check("td_block_attention",
+           lib().td_block_attention(ctypes.byref(dm), _ptr(q), _ptr(k_blk), _ptr(v_blk),
+                                    _ptr(k_ctx), _ptr(v_ctx), _ptr(ctx_len), _ptr(o), _ptr(lse),
+                                    _ptr(ws), ws.numel(), _stream(stream)))
+    return o
+
+
+def _outs(B, S, device, conf, pred, n_committed, all_done):
+    if conf is None:
+        conf = torch.empty((B, S), dtype=torch.float32, device=device)
+    if pred is None:
+        pred = torch.empty((B, S), dtype=torch.int32, device=device)
+    if n_committed is None:
+        n_committed = torch.empty((B,), dtype=torch.int32, device=device)
+    if all_done is None:
+        all_done = torch.empty((1,), dtype=torch.int32, device=device)
+    return conf, pred, n_committed, all_done
+
+
+def td_lmhead_commit(dims, h, w_lm, gamma: float, force_all: bool, tokens, masked, conf=None,
+                     pred=None, n_committed=None, all_done=None, ws=None, stream=None):
+    """Updates tokens / masked in place; returns (conf, pred, n_committed, all_done)."""
+    dm = dims if isinstance(dims, td_dims) else dims_from(dims)
+    conf, pred, n_committed, all_done = _outs(dm.B, dm.S, h.device, conf, pred, n_committed,
+                                              all_done)
+    if ws is None:
+        ws = workspace(dm, TD_FN_LMHEAD_COMMIT, h.device)
+    _check("td_lmhead_commit",
+           lib().td_lmhead_commit(ctypes.byref(dm), _ptr(h), _ptr(w_lm), gamma, int(force_all),
+                                  _ptr(tokens), _ptr(masked), _ptr(conf), _ptr(pred),
+                                  _ptr(n_committed), _ptr(all_done), _ptr(ws), ws.numel(),
+                                  _stream(stream)))
+    return conf, pred, n_committed, all_done
+
+
+def _layers(layers: Sequence[Dict[str, torch.Tensor]]):
+    arr = (td_layer * max(1, len(layers)))()
+    for i, L in enumerate(layers):
+        arr[i] = td_layer(_ptr(L["wqkv"]), _ptr(L["wo"]), _ptr(L["ada_E"]),
+                          _ptr(L.get("k_ctx")), _ptr(L.get("v_ctx")))
+    return arr
+
+
+def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tokens, masked,
+                    h=None, emb=None, pos=None, ctx_len=None, conf=None, pred=None,
+                    n_committed=None, all_done=None, ws=None, stream=None):
+    """One denoising step; tokens / masked updated in place.
+    Returns (conf, pred, n_committed, all_done)."""
+    dm = dims if isinstance(dims, td_dims) else dims_from(dims)
+    dev = w_lm.device
+    conf, pred, n_committed, all_done = _outs(dm.B, dm.S, dev, conf, pred, n_committed,
+                                              all_done)
+    if ws is None:
+        ws = workspace(dm, TD_FN_DENOISE_STEP, dev)
+    arr = _layers(layers)
+    _check("td_denoise_step",
+           lib().td_denoise_step(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(h), _ptr(emb),
+                                 _ptr(pos), _ptr(w_lm), _ptr(phi_t), t, T, gamma, _ptr(tokens),
+                                 _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
+                                 _ptr(all_done), _ptr(ws), ws.numel(), _stream(stream)))
+    return conf, pred, n_committed, all_done
+
+
+def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: float, tokens,
+                    masked, t_start: int = 1, ctx_len=None, conf=None, pred=None,
+                    n_committed=None, all_done=None, ws=None, stream=None) -> int:
+    """Runs the block decode loop in place on tokens / masked; returns the steps taken."""
+    dm = dims if isinstance(dims, td_dims) else dims_from(dims)
+    dev = w_lm.device
+    conf, pred, n_committed, all_done = _outs(dm.B, dm.S, dev, conf, pred, n_committed,
+                                              all_done)
+    if ws is None:
+        ws = workspace(dm, TD_FN_DECODE_BLOCK, dev)
+    steps = ctypes.c_int(0)
+    arr = _layers(layers)
+    _check("td_decode_block",
+           lib().td_decode_block(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(emb), _ptr(pos),
+                                 _ptr(w_lm), _ptr(phi_table), t_start, T, gamma, _ptr(tokens),
+                                 _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
+                                 _ptr(all_done), ctypes.byref(steps), _ptr(ws), ws.numel(),
+                                 _stream(stream)))
+    return steps.value

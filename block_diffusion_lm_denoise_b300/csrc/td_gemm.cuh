@@ -1,0 +1,263 @@
+// td_gemm.cuh -- persistent tcgen05 GEMM  C[M, N] = A[M, K] * B[N, K]^T  (bf16 in, fp32
+// accumulate in TMEM) with three fused epilogues:
+//   EPI_QKV    : bf16 store of the [q | k | v] projection into three row-major tensors
+//   EPI_RESID  : gated residual  h[r, n] = bf16(h[r, n] + gate[n] * C[r, n])  (in place)
+//   EPI_LMHEAD : per row and per 128/256-column vocabulary tile, (max, lowest argmax,
+//                sum of exp(z - max)) of the logits; the logits are never written.
+//
+// Roles (256 threads): warp 0 lane 0 = TMA producer; warp 1 = TMEM allocator and (lane 0)
+// MMA issuer; warps 4..7 = epilogue, thread i of warp 4+q owns accumulator row 32q+i.
+// Tiles: BM = 128 rows, BN = 128 or 256 columns, BK = 64 (one 128-byte swizzle row of bf16),
+// STAGES-deep TMA ring in shared memory, two TMEM accumulators so the epilogue of tile i
+// overlaps the MMAs of tile i+1. Work items are (m_tile, n_tile) pairs enumerated with
+// m_tile fastest and dealt round-robin to the CTAs, so the CTAs resident at any moment share
+// a narrow window of B tiles (the weights) and every weight byte leaves HBM about once.
+#pragma once
+
+#include "td_ptx.cuh"
+
+namespace td {
+
+enum { EPI_QKV = 0, EPI_RESID = 1, EPI_LMHEAD = 2 };
+
+struct GemmParams {
+  int M, N, K;
+  int m_tiles, n_tiles, items;
+  // EPI_QKV: columns [0, nq) -> q, [nq, nq + nk) -> k, [nq + nk, nq + 2 nk) -> v
+  uint16_t* q;
+  uint16_t* k;
+  uint16_t* v;
+  int nq, nk;
+  // EPI_RESID
+  uint16_t* h;
+  const float* gate;
+  // EPI_LMHEAD partials, [M][n_tiles] each
+  float* part_max;
+  int* part_arg;
+  float* part_sum;
+};
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  static constexpr int kABytes = 128 * 128;      // 128 rows x 64 bf16
+  static constexpr int kBBytes = BN * 128;       // BN rows x 64 bf16
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarOffset = STAGES * kStageBytes;
+  static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+};
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(256, 1)
+    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  using L = GemmSmem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nkb = p.K / 64;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 128);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
+        const int mt = item % p.m_tiles;
+        const int nt = item / p.m_tiles;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1, ERR_WAIT_MMA)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * L::kStageBytes;
+          mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+          tma_load_2d(sa, &tmA, &full[s], kb * 64, mt * 128);
+          tma_load_2d(sa + L::kABytes, &tmB, &full[s], kb * 64, nt * BN);
+        }
+      }
+      // On an aborted run, wait (bounded) for the loads still in flight before leaving.
+      if (!ok) {
+        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          mbar_wait(&full[j % STAGES], (j / STAGES) & 1, ERR_WAIT_TMA);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, BN, 0);
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++lt) {
+        const int acc = lt & 1;
+        const int use = lt >> 1;
+        if (lt >= 2 && !mbar_wait(&acc_empty[acc], (use & 1) ^ 1, ERR_WAIT_EPI)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, ERR_WAIT_TMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * L::kStageBytes);
+          const uint32_t b0 = a0 + L::kABytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            mma_bf16_ss(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024),
+                        sdesc_sw128(b0 + k * 32, 16, 1024), idesc, (kb | k) != 0);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[acc]);
+      }
+      // Let every MMA issued so far finish before the TMEM is released.
+      if (it > 0) mbar_wait(&empty[(it - 1) % STAGES], ((it - 1) / STAGES) & 1, ERR_WAIT_MMA);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int lt = 0;
+    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++lt) {
+      const int mt = item % p.m_tiles;
+      const int nt = item / p.m_tiles;
+      const int acc = lt & 1;
+      if (!mbar_wait(&acc_full[acc], (lt >> 1) & 1, ERR_WAIT_MMA)) break;
+      tc_fence_after();
+      const int row = mt * 128 + row_in_tile;
+      const bool row_ok = row < p.M;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+
+      float run_max = -INFINITY, run_sum = 0.f;
+      int run_arg = 0;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(taddr + c * 32, v);
+        tmem_ld_wait();
+        const int col0 = nt * BN + c * 32;
+        if constexpr (EPI == EPI_LMHEAD) {
+          // chunk maximum (lowest column on ties), then exp-sum relative to the running max
+          float cmax = -INFINITY;
+          int carg = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (col0 + j >= p.N) v[j] = -INFINITY;
+            if (v[j] > cmax) {
+              cmax = v[j];
+              carg = j;
+            }
+          }
+          if (cmax > run_max) {
+            if (run_max != -INFINITY) run_sum *= ex2_approx((run_max - cmax) * 1.4426950408889634f);
+            run_max = cmax;
+            run_arg = col0 + carg;
+          }
+          float s = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s += ex2_approx((v[j] - run_max) * 1.4426950408889634f);
+          run_sum += s;
+        } else if constexpr (EPI == EPI_QKV) {
+          if (row_ok && col0 < p.N) {
+            uint16_t* dst;
+            if (col0 < p.nq)
+              dst = p.q + (size_t)row * p.nq + col0;
+            else if (col0 < p.nq + p.nk)
+              dst = p.k + (size_t)row * p.nk + (col0 - p.nq);
+            else
+              dst = p.v + (size_t)row * p.nk + (col0 - p.nq - p.nk);
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 w;
+              w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+              w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+              w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+              w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+              d4[j] = w;
+            }
+          }
+        } else {  // EPI_RESID
+          if (row_ok && col0 < p.N) {
+            uint4* h4 = reinterpret_cast<uint4*>(p.h + (size_t)row * p.N + col0);
+            const float4* g4 = reinterpret_cast<const float4*>(p.gate + col0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 hv = h4[j];
+              const float4 ga = __ldg(&g4[2 * j]);
+              const float4 gb = __ldg(&g4[2 * j + 1]);
+              uint4 w;
+              w.x = pack_bf16x2(bf16lo_to_f32(hv.x) + ga.x * v[8 * j + 0],
+                                bf16hi_to_f32(hv.x) + ga.y * v[8 * j + 1]);
+              w.y = pack_bf16x2(bf16lo_to_f32(hv.y) + ga.z * v[8 * j + 2],
+                                bf16hi_to_f32(hv.y) + ga.w * v[8 * j + 3]);
+              w.z = pack_bf16x2(bf16lo_to_f32(hv.z) + gb.x * v[8 * j + 4],
+                                bf16hi_to_f32(hv.z) + gb.y * v[8 * j + 5]);
+              w.w = pack_bf16x2(bf16lo_to_f32(hv.w) + gb.z * v[8 * j + 6],
+                                bf16hi_to_f32(hv.w) + gb.w * v[8 * j + 7]);
+              h4[j] = w;
+            }
+          }
+        }
+      }
+      if constexpr (EPI == EPI_LMHEAD) {
+        if (row_ok) {
+          const size_t o = (size_t)row * p.n_tiles + nt;
+          p.part_max[o] = run_max;
+          p.part_arg[o] = run_arg;
+          p.part_sum[o] = run_sum;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+}  // namespace td

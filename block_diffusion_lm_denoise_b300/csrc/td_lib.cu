@@ -1,0 +1,538 @@
+// td_lib.cu -- the C ABI of the denoise step: argument validation, workspace carving,
+// TMA descriptor encoding, kernel selection and launch sequencing. Device code lives in the
+// td_*.cuh headers included below (one translation unit, so the device error word is one
+// symbol without relocatable device code).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/td.h"
+#include "td_attention.cuh"
+#include "td_gemm.cuh"
+#include "td_ptx.cuh"
+#include "td_small.cuh"
+
+namespace {
+
+using namespace td;
+
+constexpr float kLnEps = 1e-6f;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+#define TD_CUDA(call)                                   \
+  do {                                                  \
+    cudaError_t e__ = (call);                           \
+    if (e__ != cudaSuccess) return TD_ERR_CUDA;         \
+  } while (0)
+
+// ------------------------------------------------------------------------------------------
+// Driver entry point for tensor-map encoding (resolved once; no link-time libcuda).
+// ------------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor map of rank `rank` (dims innermost first, strides in bytes for dims 1..rank-1),
+// box `box`, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bd[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bd[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bd, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// ------------------------------------------------------------------------------------------
+// Validation
+// ------------------------------------------------------------------------------------------
+td_status check_dims(const td_dims* dm, bool need_model) {
+  if (!dm) return TD_ERR_INVALID_ARG;
+  if (dm->B <= 0 || dm->S <= 0 || dm->D <= 0 || dm->Hq <= 0 || dm->Hkv <= 0 || dm->Lmax < 0)
+    return TD_ERR_INVALID_ARG;
+  if (need_model && (dm->d <= 0 || dm->V <= 0 || dm->n_layers < 0)) return TD_ERR_INVALID_ARG;
+  if (dm->D != 64 && dm->D != 128) return TD_ERR_UNSUPPORTED;
+  if (dm->Hq % dm->Hkv != 0) return TD_ERR_UNSUPPORTED;
+  if (dm->S > 64) return TD_ERR_UNSUPPORTED;
+  if ((long long)dm->B * dm->S > 65536) return TD_ERR_UNSUPPORTED;
+  if (need_model && (dm->d % 64 != 0 || dm->d > 8192 || dm->V % 8 != 0)) return TD_ERR_UNSUPPORTED;
+  return TD_OK;
+}
+
+td_status check_lm_dims(const td_dims* dm) {
+  if (!dm) return TD_ERR_INVALID_ARG;
+  if (dm->B <= 0 || dm->S <= 0 || dm->d <= 0 || dm->V <= 0) return TD_ERR_INVALID_ARG;
+  if (dm->S > 64 || (long long)dm->B * dm->S > 65536) return TD_ERR_UNSUPPORTED;
+  if (dm->d % 64 != 0 || dm->V % 8 != 0) return TD_ERR_UNSUPPORTED;
+  return TD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ------------------------------------------------------------------------------------------
+// Attention plan
+// ------------------------------------------------------------------------------------------
+struct AttnPlan {
+  int G, Gc, NC, R, n_ctx_tiles, T, n_groups, ncta, max_seg;
+  long long total;
+  size_t part_o_bytes, part_ml_bytes;
+};
+
+AttnPlan plan_attention(const td_dims* dm, int nsm) {
+  AttnPlan a{};
+  a.G = dm->Hq / dm->Hkv;
+  a.Gc = 1;
+  for (int c = a.G; c >= 1; --c)
+    if (a.G % c == 0 && dm->S * c <= 256) { a.Gc = c; break; }
+  a.NC = a.G / a.Gc;
+  a.R = dm->S * a.Gc;
+  a.n_ctx_tiles = (dm->Lmax + 63) / 64;
+  a.T = a.n_ctx_tiles + 1;
+  a.n_groups = dm->B * dm->Hkv * a.NC;
+  a.total = (long long)a.n_groups * a.T;
+  if (a.n_groups <= nsm && a.n_groups * 5 >= nsm * 4)
+    a.ncta = a.n_groups;                       // one CTA per row group: no merge pass
+  else
+    a.ncta = (int)std::min<long long>(nsm, a.total);
+  const long long per = (a.total + a.ncta - 1) / a.ncta;
+  a.max_seg = (int)((per + a.T - 1) / a.T) + 1;
+  const size_t recs = (size_t)a.ncta * a.max_seg;
+  a.part_o_bytes = align_up(recs * a.R * dm->D * sizeof(float));
+  a.part_ml_bytes = align_up(recs * a.R * 2 * sizeof(float));
+  return a;
+}
+
+size_t attn_ws_bytes(const td_dims* dm, int nsm) {
+  const AttnPlan a = plan_attention(dm, nsm);
+  return a.part_o_bytes + a.part_ml_bytes;
+}
+
+// ------------------------------------------------------------------------------------------
+// LM head plan
+// ------------------------------------------------------------------------------------------
+int lm_bn(int M) { return M <= 128 ? 128 : 256; }
+
+size_t lm_ws_bytes(int M, int V) {
+  const int nt = (V + lm_bn(M) - 1) / lm_bn(M);
+  const size_t part = (size_t)M * nt;
+  return align_up(part * 4) * 3 + kAlign;   // max, arg, sum, counters
+}
+
+// ------------------------------------------------------------------------------------------
+// Launch helpers
+// ------------------------------------------------------------------------------------------
+template <int BN, int STAGES, int EPI>
+td_status launch_gemm(const void* A, const void* Bm, int M, int N, int K, GemmParams gp,
+                      cudaStream_t st, int nsm) {
+  using L = GemmSmem<BN, STAGES>;
+  CUtensorMap ma, mb;
+  const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)K * 2};
+  const uint32_t ba[2] = {64, 128};
+  const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)K * 2};
+  const uint32_t bb[2] = {64, (uint32_t)BN};
+  if (!make_map(&ma, A, 2, da, sa, ba) || !make_map(&mb, Bm, 2, db, sb, bb)) return TD_ERR_CUDA;
+  gp.M = M;
+  gp.N = N;
+  gp.K = K;
+  gp.m_tiles = (M + 127) / 128;
+  gp.n_tiles = (N + BN - 1) / BN;
+  gp.items = gp.m_tiles * gp.n_tiles;
+  auto kern = gemm_tn_kernel<BN, STAGES, EPI>;
+  static bool attr_done[3] = {false, false, false};
+  (void)attr_done;
+  TD_CUDA(set_smem(kern, L::kBytes));
+  const int grid = std::min(gp.items, nsm);
+  kern<<<grid, 256, L::kBytes, st>>>(ma, mb, gp);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
+}
+
+template <int EPI>
+td_status gemm_dispatch(const void* A, const void* Bm, int M, int N, int K, GemmParams gp,
+                        cudaStream_t st, int nsm, int bn) {
+  if (bn == 128) return launch_gemm<128, 6, EPI>(A, Bm, M, N, K, gp, st, nsm);
+  return launch_gemm<256, 4, EPI>(A, Bm, M, N, K, gp, st, nsm);
+}
+
+td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, float gamma,
+                            int force_all, int* tokens, unsigned char* masked, float* conf,
+                            int* pred, int* n_committed, int* all_done, void* ws,
+                            cudaStream_t st, int nsm) {
+  const int M = dm->B * dm->S;
+  const int V = dm->V;
+  const int bn = lm_bn(M);
+  const int nt = (V + bn - 1) / bn;
+  const size_t part = (size_t)M * nt;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* pmax = reinterpret_cast<float*>(w);
+  int* parg = reinterpret_cast<int*>(w + align_up(part * 4));
+  float* psum = reinterpret_cast<float*>(w + 2 * align_up(part * 4));
+  int* counters = reinterpret_cast<int*>(w + 3 * align_up(part * 4));
+  GemmParams gp{};
+  gp.part_max = pmax;
+  gp.part_arg = parg;
+  gp.part_sum = psum;
+  td_status s = gemm_dispatch<EPI_LMHEAD>(h, w_lm, M, V, dm->d, gp, st, nsm, bn);
+  if (s != TD_OK) return s;
+  TD_CUDA(cudaMemsetAsync(counters, 0, 2 * sizeof(int), st));
+  merge_commit_kernel<<<dm->B, kCommitThreads, 0, st>>>(pmax, parg, psum, nt, dm->S, gamma,
+                                                         force_all, tokens, masked, conf, pred,
+                                                         n_committed, all_done, counters);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
+}
+
+td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, const void* v_blk,
+                        const void* k_ctx, const void* v_ctx, const int* ctx_len, void* o,
+                        float* lse, void* ws, cudaStream_t st, int nsm) {
+  const AttnPlan a = plan_attention(dm, nsm);
+  const int D = dm->D;
+  CUtensorMap mq, mkc, mvc, mkb, mvb;
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)dm->Hq, (uint64_t)dm->S, (uint64_t)dm->B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)dm->Hq * D * 2,
+                             (uint64_t)dm->S * dm->Hq * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)a.Gc, (uint32_t)dm->S, 1};
+    if (!make_map(&mq, q, 4, dims, str, box)) return TD_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)dm->Hkv, (uint64_t)dm->S, (uint64_t)dm->B};
+    const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)dm->Hkv * D * 2,
+                             (uint64_t)dm->S * dm->Hkv * D * 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)dm->S, 1};
+    if (!make_map(&mkb, k_blk, 4, dims, str, box) || !make_map(&mvb, v_blk, 4, dims, str, box))
+      return TD_ERR_CUDA;
+  }
+  {
+    // an empty cache still needs a well-formed (never used) descriptor
+    const bool empty = dm->Lmax == 0;
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)(empty ? 1 : dm->Lmax),
+                              (uint64_t)(empty ? 1 : dm->B * dm->Hkv)};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)(empty ? 1 : dm->Lmax) * D * 2};
+    const uint32_t box[3] = {64, 64, 1};
+    const void* kb = empty ? k_blk : k_ctx;
+    const void* vb = empty ? v_blk : v_ctx;
+    if (!make_map(&mkc, kb, 3, dims, str, box) || !make_map(&mvc, vb, 3, dims, str, box))
+      return TD_ERR_CUDA;
+  }
+  AttnParams p{};
+  p.B = dm->B; p.S = dm->S; p.Hq = dm->Hq; p.Hkv = dm->Hkv; p.D = D; p.Lmax = dm->Lmax;
+  p.G = a.G; p.Gc = a.Gc; p.NC = a.NC; p.R = a.R;
+  p.n_ctx_tiles = a.n_ctx_tiles; p.T = a.T; p.n_groups = a.n_groups; p.total = a.total;
+  p.max_seg = a.max_seg;
+  p.ctx_len = ctx_len;
+  p.part_o = static_cast<float*>(ws);
+  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + a.part_o_bytes);
+  p.out = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  if (D == 128) {
+    TD_CUDA(set_smem(attn_fused_kernel<128>, AttnSmem<128>::kBytes));
+    attn_fused_kernel<128><<<a.ncta, kAttnThreads, AttnSmem<128>::kBytes, st>>>(mq, mkc, mvc, mkb,
+                                                                               mvb, p);
+  } else {
+    TD_CUDA(set_smem(attn_fused_kernel<64>, AttnSmem<64>::kBytes));
+    attn_fused_kernel<64><<<a.ncta, kAttnThreads, AttnSmem<64>::kBytes, st>>>(mq, mkc, mvc, mkb,
+                                                                             mvb, p);
+  }
+  TD_CUDA(cudaGetLastError());
+  if (!(a.n_groups == a.ncta)) {
+    attn_merge_kernel<<<a.n_groups, 256, 0, st>>>(p, a.ncta);
+    TD_CUDA(cudaGetLastError());
+  }
+  return TD_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// Denoise-step workspace
+// ------------------------------------------------------------------------------------------
+struct StepWs {
+  uint16_t *h, *xmod, *q, *k, *v, *o;
+  float* gate;
+  void* attn;
+  void* lm;
+  size_t total;
+};
+
+StepWs carve_step(const td_dims* dm, void* base, int nsm) {
+  StepWs w{};
+  const size_t M = (size_t)dm->B * dm->S;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  const size_t o_h = take(M * dm->d * 2), o_x = take(M * dm->d * 2);
+  const size_t o_q = take(M * dm->Hq * dm->D * 2), o_k = take(M * dm->Hkv * dm->D * 2),
+               o_v = take(M * dm->Hkv * dm->D * 2), o_o = take(M * dm->Hq * dm->D * 2);
+  const size_t o_g = take((size_t)dm->d * 4);
+  const size_t o_a = take(attn_ws_bytes(dm, nsm));
+  const size_t o_l = take(lm_ws_bytes((int)M, dm->V));
+  w.total = off;
+  if (base) {
+    uint8_t* b = static_cast<uint8_t*>(base);
+    w.h = reinterpret_cast<uint16_t*>(b + o_h);
+    w.xmod = reinterpret_cast<uint16_t*>(b + o_x);
+    w.q = reinterpret_cast<uint16_t*>(b + o_q);
+    w.k = reinterpret_cast<uint16_t*>(b + o_k);
+    w.v = reinterpret_cast<uint16_t*>(b + o_v);
+    w.o = reinterpret_cast<uint16_t*>(b + o_o);
+    w.gate = reinterpret_cast<float*>(b + o_g);
+    w.attn = b + o_a;
+    w.lm = b + o_l;
+  }
+  return w;
+}
+
+td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len, const void* h,
+                   const void* emb, const void* pos, const void* w_lm, const float* phi_t,
+                   int t, int T, float gamma, int* tokens, unsigned char* masked, float* conf,
+                   int* pred, int* n_committed, int* all_done, void* ws, cudaStream_t st,
+                   int nsm) {
+  const StepWs w = carve_step(dm, ws, nsm);
+  const int M = dm->B * dm->S;
+  const int d = dm->d;
+  if (h == nullptr) {
+    embed_kernel<<<M, 256, 0, st>>>(tokens, static_cast<const uint16_t*>(emb),
+                                    static_cast<const uint16_t*>(pos), w.h, dm->S, d, dm->V);
+  } else {
+    TD_CUDA(cudaMemcpyAsync(w.h, h, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st));
+  }
+  TD_CUDA(cudaGetLastError());
+  const int nq = dm->Hq * dm->D, nk = dm->Hkv * dm->D;
+  const int bn = M >= 512 ? 256 : 128;
+  for (int l = 0; l < dm->n_layers; ++l) {
+    const td_layer& L = layers[l];
+    adaln_modulate_kernel<<<M, kAdaThreads, 0, st>>>(w.h, L.ada_E, phi_t, d, kLnEps, w.xmod,
+                                                     w.gate);
+    TD_CUDA(cudaGetLastError());
+    GemmParams g1{};
+    g1.q = w.q; g1.k = w.k; g1.v = w.v; g1.nq = nq; g1.nk = nk;
+    td_status s = gemm_dispatch<EPI_QKV>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn);
+    if (s != TD_OK) return s;
+    s = run_attention(dm, w.q, w.k, w.v, L.k_ctx, L.v_ctx, ctx_len, w.o, nullptr, w.attn, st,
+                      nsm);
+    if (s != TD_OK) return s;
+    GemmParams g2{};
+    g2.h = w.h; g2.gate = w.gate;
+    s = gemm_dispatch<EPI_RESID>(w.o, L.wo, M, d, nq, g2, st, nsm, bn);
+    if (s != TD_OK) return s;
+  }
+  return run_lmhead_commit(dm, w.h, w_lm, gamma, t == T ? 1 : 0, tokens, masked, conf, pred,
+                           n_committed, all_done, w.lm, st, nsm);
+}
+
+td_status check_layers(const td_dims* dm, const td_layer* layers) {
+  if (dm->n_layers > 0 && !layers) return TD_ERR_INVALID_ARG;
+  for (int l = 0; l < dm->n_layers; ++l) {
+    const td_layer& L = layers[l];
+    if (!L.wqkv || !L.wo || !L.ada_E) return TD_ERR_INVALID_ARG;
+    if (dm->Lmax > 0 && (!L.k_ctx || !L.v_ctx)) return TD_ERR_INVALID_ARG;
+    if (!aligned16(L.wqkv) || !aligned16(L.wo) || !aligned16(L.ada_E) ||
+        (dm->Lmax > 0 && (!aligned16(L.k_ctx) || !aligned16(L.v_ctx))))
+      return TD_ERR_INVALID_ARG;
+  }
+  return TD_OK;
+}
+
+bool ws_ok(const void* ws, size_t have, size_t need) {
+  if (need == 0) return true;
+  return ws != nullptr && have >= need && (reinterpret_cast<uintptr_t>(ws) % kAlign) == 0;
+}
+
+}  // namespace
+
+// ==========================================================================================
+// C ABI
+// ==========================================================================================
+extern "C" {
+
+const char* td_status_string(td_status s) {
+  switch (s) {
+    case TD_OK: return "TD_OK";
+    case TD_ERR_INVALID_ARG: return "TD_ERR_INVALID_ARG";
+    case TD_ERR_WORKSPACE: return "TD_ERR_WORKSPACE";
+    case TD_ERR_UNSUPPORTED: return "TD_ERR_UNSUPPORTED";
+    case TD_ERR_CUDA: return "TD_ERR_CUDA";
+    case TD_ERR_NOT_CONVERGED: return "TD_ERR_NOT_CONVERGED";
+    case TD_ERR_DEVICE_TIMEOUT: return "TD_ERR_DEVICE_TIMEOUT";
+  }
+  return "TD_STATUS_UNKNOWN";
+}
+
+size_t td_workspace_size(const td_dims* dm, int fn) {
+  const int nsm = sm_count();
+  switch (fn) {
+    case TD_FN_ADALN_MODULATE:
+      return 0;
+    case TD_FN_BLOCK_ATTENTION:
+      if (check_dims(dm, false) != TD_OK) return (size_t)-1;
+      return attn_ws_bytes(dm, nsm);
+    case TD_FN_LMHEAD_COMMIT:
+      if (check_lm_dims(dm) != TD_OK) return (size_t)-1;
+      return lm_ws_bytes(dm->B * dm->S, dm->V);
+    case TD_FN_DENOISE_STEP:
+    case TD_FN_DECODE_BLOCK:
+      if (check_dims(dm, true) != TD_OK) return (size_t)-1;
+      return carve_step(dm, nullptr, nsm).total;
+  }
+  return (size_t)-1;
+}
+
+td_status td_adaln_modulate(const void* h, const float* E, const float* phi, int rows, int d,
+                            float eps, void* x_mod, void* stream) {
+  if (!h || !E || !phi || !x_mod || rows <= 0 || d <= 0 || !(eps >= 0.f))
+    return TD_ERR_INVALID_ARG;
+  if (d % 8 != 0 || d > 8 * kAdaThreads * kAdaMaxVec) return TD_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(x_mod)) return TD_ERR_INVALID_ARG;
+  adaln_modulate_kernel<<<rows, kAdaThreads, 0, (cudaStream_t)stream>>>(
+      static_cast<const uint16_t*>(h), E, phi, d, eps, static_cast<uint16_t*>(x_mod), nullptr);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
+}
+
+td_status td_block_attention(const td_dims* dims, const void* q, const void* k_blk,
+                             const void* v_blk, const void* k_ctx, const void* v_ctx,
+                             const int* ctx_len, void* o, float* lse, void* ws, size_t ws_bytes,
+                             void* stream) {
+  td_status s = check_dims(dims, false);
+  if (s != TD_OK) return s;
+  if (!q || !k_blk || !v_blk || !o) return TD_ERR_INVALID_ARG;
+  if (dims->Lmax > 0 && (!k_ctx || !v_ctx)) return TD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_blk) || !aligned16(v_blk) || !aligned16(o) ||
+      (dims->Lmax > 0 && (!aligned16(k_ctx) || !aligned16(v_ctx))))
+    return TD_ERR_INVALID_ARG;
+  const int nsm = sm_count();
+  if (!ws_ok(ws, ws_bytes, attn_ws_bytes(dims, nsm))) return TD_ERR_WORKSPACE;
+  return run_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, o, lse, ws,
+                       (cudaStream_t)stream, nsm);
+}
+
+td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm, float gamma,
+                           int force_all, int* tokens, unsigned char* masked, float* conf,
+                           int* pred, int* n_committed, int* all_done, void* ws, size_t ws_bytes,
+                           void* stream) {
+  td_status s = check_lm_dims(dims);
+  if (s != TD_OK) return s;
+  if (!h || !w_lm || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
+    return TD_ERR_INVALID_ARG;
+  if (std::isnan(gamma)) return TD_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w_lm)) return TD_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, lm_ws_bytes(dims->B * dims->S, dims->V))) return TD_ERR_WORKSPACE;
+  return run_lmhead_commit(dims, h, w_lm, gamma, force_all, tokens, masked, conf, pred,
+                           n_committed, all_done, ws, (cudaStream_t)stream, sm_count());
+}
+
+td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int* ctx_len,
+                          const void* h, const void* emb, const void* pos, const void* w_lm,
+                          const float* phi_t, int t, int T, float gamma, int* tokens,
+                          unsigned char* masked, float* conf, int* pred, int* n_committed,
+                          int* all_done, void* ws, size_t ws_bytes, void* stream) {
+  td_status s = check_dims(dims, true);
+  if (s != TD_OK) return s;
+  if ((s = check_layers(dims, layers)) != TD_OK) return s;
+  if (!w_lm || !phi_t || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
+    return TD_ERR_INVALID_ARG;
+  if (!h && (!emb || !pos)) return TD_ERR_INVALID_ARG;
+  if (t < 1 || T < 1 || t > T || std::isnan(gamma)) return TD_ERR_INVALID_ARG;
+  const int nsm = sm_count();
+  if (!ws_ok(ws, ws_bytes, carve_step(dims, nullptr, nsm).total)) return TD_ERR_WORKSPACE;
+  return run_step(dims, layers, ctx_len, h, emb, pos, w_lm, phi_t, t, T, gamma, tokens, masked,
+                  conf, pred, n_committed, all_done, ws, (cudaStream_t)stream, nsm);
+}
+
+td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
+                          const void* emb, const void* pos, const void* w_lm,
+                          const float* phi_table, int t_start, int T, float gamma, int* tokens,
+                          unsigned char* masked, float* conf, int* pred, int* n_committed,
+                          int* all_done, int* steps_taken, void* ws, size_t ws_bytes,
+                          void* stream) {
+  td_status s = check_dims(dims, true);
+  if (s != TD_OK) return s;
+  if ((s = check_layers(dims, layers)) != TD_OK) return s;
+  if (!emb || !pos || !w_lm || !phi_table || !tokens || !masked || !conf || !pred ||
+      !n_committed || !all_done || !steps_taken)
+    return TD_ERR_INVALID_ARG;
+  if (t_start < 1 || T < 1 || std::isnan(gamma)) return TD_ERR_INVALID_ARG;
+  const int nsm = sm_count();
+  if (!ws_ok(ws, ws_bytes, carve_step(dims, nullptr, nsm).total)) return TD_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  *steps_taken = 0;
+  // nothing masked on entry: nothing to do
+  {
+    std::vector<unsigned char> m((size_t)dims->B * dims->S);
+    TD_CUDA(cudaMemcpyAsync(m.data(), masked, m.size(), cudaMemcpyDeviceToHost, st));
+    TD_CUDA(cudaStreamSynchronize(st));
+    bool any = false;
+    for (unsigned char c : m) any |= (c != 0);
+    if (!any) return TD_OK;
+  }
+  int done = 0;
+  for (int t = t_start; t <= T; ++t) {
+    s = run_step(dims, layers, ctx_len, nullptr, emb, pos, w_lm,
+                 phi_table + (size_t)(t - 1) * 6 * dims->d, t, T, gamma, tokens, masked, conf,
+                 pred, n_committed, all_done, ws, st, nsm);
+    if (s != TD_OK) return s;
+    TD_CUDA(cudaMemcpyAsync(&done, all_done, sizeof(int), cudaMemcpyDeviceToHost, st));
+    TD_CUDA(cudaStreamSynchronize(st));
+    ++*steps_taken;
+    if (done) break;
+  }
+  return done ? TD_OK : TD_ERR_NOT_CONVERGED;
+}
+
+td_status td_device_error(int* code) {
+  if (!code) return TD_ERR_INVALID_ARG;
+  TD_CUDA(cudaDeviceSynchronize());
+  unsigned int v = 0, zero = 0;
+  TD_CUDA(cudaMemcpyFromSymbol(&v, td::g_error_word, sizeof(v)));
+  TD_CUDA(cudaMemcpyToSymbol(td::g_error_word, &zero, sizeof(zero)));
+  *code = (int)v;
+  return TD_OK;
+}
+
+}  // extern "C"

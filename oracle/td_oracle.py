@@ -249,7 +249,12 @@ def embed(tokens, emb, pos) -> np.ndarray:
     """h0[b, i] = bf16(emb[tokens[b, i]] + pos[i]); returns [B*S, d]."""
     tokens = np.asarray(tokens)
     B, S = tokens.shape
-    e = as_f64(emb)[tokens.reshape(-1)]
+    idx = tokens.reshape(-1).astype(np.int64)
+    if hasattr(emb, "detach"):                      # gather the rows before widening
+        import torch
+        e = as_f64(emb[torch.from_numpy(idx).to(emb.device)])
+    else:
+        e = as_f64(np.asarray(emb)[idx])
     p = np.tile(as_f64(pos)[:S], (B, 1))
     return bf16_round(e + p)
 

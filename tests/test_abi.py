@@ -1,0 +1,81 @@
+"""The C ABI library: it loads, exports every function include/td.h declares, and rejects
+bad arguments on the host before launching anything (CPU, no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import block_diffusion_lm_denoise_b300 as td
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "td.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(td_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(td.LIB_PATH):
+        from block_diffusion_lm_denoise_b300 import build
+        build.build()
+    return td.lib()
+
+
+def test_every_declared_function_is_exported(lib):
+    declared = _header_functions()
+    assert set(declared) == set(td.EXPORTED), declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["TD_OK", "TD_ERR_INVALID_ARG", "TD_ERR_WORKSPACE",
+                                 "TD_ERR_UNSUPPORTED", "TD_ERR_CUDA", "TD_ERR_NOT_CONVERGED",
+                                 "TD_ERR_DEVICE_TIMEOUT"]):
+        assert lib.td_status_string(code).decode() == name
+
+
+def test_workspace_sizes_and_unsupported_shapes(lib):
+    ok = td.make_dims(B=64, S=16, d=4096, Hq=32, Hkv=2, D=128, V=131072, Lmax=8192, n_layers=6)
+    for fn in (td.TD_FN_BLOCK_ATTENTION, td.TD_FN_LMHEAD_COMMIT, td.TD_FN_DENOISE_STEP,
+               td.TD_FN_DECODE_BLOCK):
+        assert td.td_workspace_size(ok, fn) > 0
+    assert td.td_workspace_size(ok, td.TD_FN_ADALN_MODULATE) == 0
+    for bad in (dict(D=96), dict(Hq=30, Hkv=4), dict(S=65), dict(d=100)):
+        dm = td.make_dims(**{**dict(B=2, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64,
+                                     n_layers=1), **bad})
+        with pytest.raises(td.TdError):
+            td.td_workspace_size(dm, td.TD_FN_DENOISE_STEP)
+
+
+def test_null_pointers_are_rejected_before_any_launch(lib):
+    dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=1)
+    # every pointer null: validation must fail first
+    assert lib.td_block_attention(ctypes.byref(dm), None, None, None, None, None, None, None,
+                                  None, None, 0, None) == 1
+    assert lib.td_lmhead_commit(ctypes.byref(dm), None, None, 0.8, 0, None, None, None, None,
+                                None, None, None, 0, None) == 1
+    assert lib.td_adaln_modulate(None, None, None, 4, 256, 1e-6, None, None) == 1
+    steps = ctypes.c_int(0)
+    assert lib.td_decode_block(ctypes.byref(dm), None, None, None, None, None, None, 1, 16,
+                               0.8, None, None, None, None, None, None, ctypes.byref(steps),
+                               None, 0, None) == 1
+    # shapes outside the kernels' limits
+    bad = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=80, V=1024, Lmax=64, n_layers=1)
+    fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the shape check fails first
+    assert lib.td_block_attention(ctypes.byref(bad), fake, fake, fake, fake, fake, None, fake,
+                                  None, fake, 1 << 20, None) == 3
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake device pointers only without a GPU")
+def test_undersized_workspace_is_rejected(lib):
+    dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=1)
+    fake = ctypes.c_void_p(1 << 40)
+    assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None, fake,
+                                  None, fake, 16, None) == 2

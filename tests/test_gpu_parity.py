@@ -1,0 +1,333 @@
+"""GPU parity: every entry point of the C ABI against the fp64 oracle on seeded inputs.
+
+Small cases span several tiles and ragged tails and run the oracle in full; full-size cases
+(the mid-size step, the attention sweep, the LM-head sweep, the decode loop) compare
+sampled rows / sequences, which the oracle computes one by one.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_diffusion_lm_denoise_b300 as td
+import oracle
+from block_diffusion_lm_denoise_b300 import synth
+from parity_util import attention_close, compare_commit
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    return oracle.as_f64(t)
+
+
+def _no_device_error():
+    assert td.td_device_error() == 0
+
+
+# ------------------------------------------------------------------------------ adaLN
+
+@pytest.mark.parametrize("rows,d", [(16, 256), (37, 4096), (130, 1024)])
+def test_adaln_modulate_matches_oracle(cuda_device, rows, d):
+    h = synth.normal((rows, d), 1.7, 5, f"h{rows}", cuda_device)
+    E = synth.normal((6, d), 0.02, 5, "E", cuda_device, torch.float32)
+    phi = synth.normal((6, d), 0.25, 5, "phi", cuda_device, torch.float32)
+    out = td.td_adaln_modulate(h, E, phi)
+    torch.cuda.synchronize()
+    _no_device_error()
+    ref = oracle.adaln_modulate(h, E, phi)
+    got = _np(out)
+    diff = got != ref
+    # fp32 statistics vs fp64: a value within ~1e-6 relative of a bf16 rounding boundary may
+    # round the other way; such flips are single-ulp and rare
+    ulp = np.abs(ref) * 2.0**-7 + 1e-30
+    assert (np.abs(got - ref) <= ulp).all()
+    assert diff.mean() < 2e-3, diff.mean()
+
+
+# ------------------------------------------------------------------------------ attention
+
+ATTN_CASES = [
+    # B, S, Hq, Hkv, D, Lmax, ctx_len
+    (1, 16, 4, 1, 64, 64, None),              # the tiny step's shape
+    (2, 16, 32, 2, 128, 300, None),           # ragged last context tile, GQA 16
+    (3, 16, 8, 2, 128, 200, [200, 0, 77]),    # ragged per-sequence lengths incl. empty
+    (2, 16, 32, 2, 128, 0, None),             # no context at all: block only
+    (2, 4, 8, 8, 64, 130, None),              # MHA, tiny block
+    (1, 32, 32, 2, 128, 190, None),           # S*G = 512 > 256: two row groups per KV head
+    (1, 1, 4, 1, 64, 0, None),                # one key: output == v exactly
+]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,D,Lmax,ctx", ATTN_CASES)
+def test_block_attention_matches_oracle(cuda_device, B, S, Hq, Hkv, D, Lmax, ctx):
+    seed = 11
+    q = synth.normal((B, S, Hq, D), 1.0, seed, "q", cuda_device)
+    kb = synth.normal((B, S, Hkv, D), 1.0, seed, "kb", cuda_device)
+    vb = synth.normal((B, S, Hkv, D), 1.0, seed, "vb", cuda_device)
+    kc = synth.normal((B, Hkv, max(Lmax, 1), D), 1.0, seed, "kc", cuda_device)[:, :, :Lmax].contiguous()
+    vc = synth.normal((B, Hkv, max(Lmax, 1), D), 1.0, seed, "vc", cuda_device)[:, :, :Lmax].contiguous()
+    ctx_t = None if ctx is None else torch.tensor(ctx, dtype=torch.int32, device=cuda_device)
+    dims = td.make_dims(B=B, S=S, d=64, Hq=Hq, Hkv=Hkv, D=D, V=8, Lmax=Lmax, n_layers=1)
+    lse = torch.empty((B, S, Hq), dtype=torch.float32, device=cuda_device)
+    o = td.td_block_attention(dims, q, kb, vb, kc if Lmax else None, vc if Lmax else None,
+                              ctx_t, lse=lse)
+    torch.cuda.synchronize()
+    _no_device_error()
+    o_ref, lse_ref = oracle.block_attention(q, kb, vb, kc, vc, ctx)
+    ok, worst = attention_close(_np(o), o_ref)
+    assert ok, worst
+    assert np.abs(_np(lse) - lse_ref).max() < 1e-3
+    if S == 1 and Lmax == 0:
+        assert torch.equal(o[0, 0, 0], vb[0, 0, 0]) and torch.equal(o[0, 0, 3], vb[0, 0, 0])
+
+
+@pytest.mark.parametrize("L", [512, 2048, 8192, 32768])
+def test_attention_sweep_full_size_sampled(cuda_device, L):
+    wl = synth.attention_sweep(L, cuda_device)
+    lay = wl.layers[0]
+    dm = wl.dims
+    o = td.td_block_attention(dm.as_dict(), lay["q"], lay["k_blk"], lay["v_blk"], lay["k_ctx"],
+                              lay["v_ctx"])
+    torch.cuda.synchronize()
+    _no_device_error()
+    for b in (0, dm.B - 1):
+        o_ref, _ = oracle.block_attention(lay["q"][b:b + 1], lay["k_blk"][b:b + 1],
+                                          lay["v_blk"][b:b + 1], lay["k_ctx"][b:b + 1],
+                                          lay["v_ctx"][b:b + 1])
+        ok, worst = attention_close(_np(o[b:b + 1]), o_ref)
+        assert ok, (b, worst)
+
+
+# ------------------------------------------------------------------------------ LM head + commit
+
+def _lm_case(cuda_device, M, S, V, d, gamma, seed=3, w_scale=0.02, zero_w=False):
+    B = M // S
+    w = torch.zeros((V, d), dtype=torch.bfloat16, device=cuda_device) if zero_w else \
+        synth.normal((V, d), w_scale, seed, "w_lm", cuda_device)
+    temp = synth.uniform((M, 1), 0.2, 2.0, seed, "temp", cuda_device)
+    h = (synth.normal((M, d), 1.0, seed, "h", cuda_device, torch.float32) / temp).to(torch.bfloat16)
+    masked = synth.bernoulli((B, S), 0.8, seed, "m", cuda_device).to(torch.uint8)
+    tokens = torch.where(masked.bool(), torch.full((B, S), V, dtype=torch.int32, device=cuda_device),
+                         synth.integers((B, S), V, seed, "t", cuda_device))
+    return h, w, tokens, masked
+
+
+@pytest.mark.parametrize("M,S,V,d,gamma", [(16, 16, 1024, 256, 0.8), (48, 4, 1000, 128, 0.5),
+                                           (256, 32, 2048, 512, 0.95), (320, 16, 4096, 256, 0.8)])
+def test_lmhead_commit_matches_oracle(cuda_device, M, S, V, d, gamma):
+    h, w, tokens, masked = _lm_case(cuda_device, M, S, V, d, gamma, w_scale=0.3)
+    m0 = masked.clone()
+    t0 = tokens.clone()
+    dims = td.make_dims(B=M // S, S=S, d=d, Hq=1, Hkv=1, D=64, V=V, Lmax=0, n_layers=0)
+    conf, pred, ncom, done = td.td_lmhead_commit(dims, h, w, gamma, False, tokens, masked)
+    torch.cuda.synchronize()
+    _no_device_error()
+    c_ref, p_ref, gap, _ = oracle.lmhead_confidence(h, w)
+    B = M // S
+    tok_ref, msk_ref, n_ref, _ = oracle.commit(c_ref.reshape(B, S), p_ref.reshape(B, S),
+                                               t0.cpu().numpy(), m0.cpu().numpy().astype(bool),
+                                               gamma, False)
+    rep = compare_commit(dict(conf=c_ref.reshape(B, S), pred=p_ref.reshape(B, S),
+                              gap=gap.reshape(B, S), tokens=tok_ref, masked=msk_ref),
+                         dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                              tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
+                         m0.cpu().numpy(), gamma)
+    assert int(done.item()) == int(not msk_ref.any())
+    print(rep)
+
+
+def test_lmhead_zero_weights_closed_form(cuda_device):
+    # W = 0: every logit is 0, conf = 1/V exactly, pred = 0; gamma = 1/V commits everything
+    M, S, V, d = 64, 16, 1024, 256
+    h, w, tokens, masked = _lm_case(cuda_device, M, S, V, d, 0.8, zero_w=True)
+    masked.fill_(1)
+    dims = td.make_dims(B=M // S, S=S, d=d, Hq=1, Hkv=1, D=64, V=V, Lmax=0, n_layers=0)
+    conf, pred, ncom, done = td.td_lmhead_commit(dims, h, w, 1.0 / V, False, tokens, masked)
+    torch.cuda.synchronize()
+    assert torch.all(conf == 1.0 / V) and torch.all(pred == 0)
+    assert torch.all(masked == 0) and torch.all(ncom == S) and int(done.item()) == 1
+    assert torch.all(tokens == 0)
+
+
+def test_lmhead_gamma_above_one_commits_lowest_index_of_identical_rows(cuda_device):
+    M, S, V, d = 32, 16, 512, 128
+    w = synth.normal((V, d), 0.3, 9, "w", cuda_device)
+    h = synth.normal((1, d), 1.0, 9, "h", cuda_device).repeat(M, 1)   # identical rows
+    tokens = torch.full((M // S, S), V, dtype=torch.int32, device=cuda_device)
+    masked = torch.ones((M // S, S), dtype=torch.uint8, device=cuda_device)
+    dims = td.make_dims(B=M // S, S=S, d=d, Hq=1, Hkv=1, D=64, V=V, Lmax=0, n_layers=0)
+    conf, pred, ncom, done = td.td_lmhead_commit(dims, h, w, 1.5, False, tokens, masked)
+    torch.cuda.synchronize()
+    assert torch.all(conf == conf[0, 0])                 # identical rows, identical bits
+    assert torch.all(ncom == 1) and torch.all(masked[:, 0] == 0) and torch.all(masked[:, 1:] == 1)
+    assert int(done.item()) == 0
+
+
+@pytest.mark.parametrize("M,S,gamma", [(16, 16, 0.8), (256, 4, 0.5), (1024, 16, 0.8),
+                                       (4096, 32, 0.95)])
+def test_lmhead_sweep_full_size_sampled(cuda_device, M, S, gamma):
+    wl = synth.lmhead_sweep(M, S, gamma, cuda_device)
+    dm = wl.dims
+    t0 = wl.tokens.clone()
+    m0 = wl.masked.clone()
+    conf, pred, ncom, done = td.td_lmhead_commit(dm.as_dict(), wl.h, wl.w_lm, gamma, False,
+                                                 wl.tokens, wl.masked)
+    torch.cuda.synchronize()
+    _no_device_error()
+    seqs = sorted({0, dm.B // 2, dm.B - 1})
+    rows = [b * S + i for b in seqs for i in range(S)]
+    c_ref, p_ref, gap, _ = oracle.lmhead_confidence(wl.h, wl.w_lm, rows=rows)
+    nb = len(seqs)
+    tok_ref, msk_ref, _, _ = oracle.commit(c_ref.reshape(nb, S), p_ref.reshape(nb, S),
+                                           t0[seqs].cpu().numpy(),
+                                           m0[seqs].cpu().numpy().astype(bool), gamma, False)
+    compare_commit(dict(conf=c_ref.reshape(nb, S), pred=p_ref.reshape(nb, S),
+                        gap=gap.reshape(nb, S), tokens=tok_ref, masked=msk_ref),
+                   dict(conf=conf[seqs].cpu().numpy(), pred=pred[seqs].cpu().numpy(),
+                        tokens=wl.tokens[seqs].cpu().numpy(), masked=wl.masked[seqs].cpu().numpy()),
+                   m0[seqs].cpu().numpy(), gamma)
+    # every sequence commits at least one position, none reverts
+    assert torch.all(ncom >= 1)
+    assert not torch.any((m0 == 0) & (wl.masked == 1))
+
+
+# ------------------------------------------------------------------------------ whole step
+
+def _oracle_layers(wl, rows=None):
+    out = []
+    for L in wl.layers:
+        d = dict(L)
+        if rows is not None:
+            d["k_ctx"] = L["k_ctx"][rows]
+            d["v_ctx"] = L["v_ctx"][rows]
+        out.append(d)
+    return out
+
+
+def test_denoise_step_tiny_matches_oracle(cuda_device):
+    wl = synth.tiny_step(cuda_device)
+    dm = wl.dims
+    t0, m0 = wl.tokens.clone(), wl.masked.clone()
+    conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), wl.layers, wl.w_lm,
+                                                wl.phi_table[wl.t - 1], wl.t, wl.T, wl.gamma,
+                                                wl.tokens, wl.masked, h=wl.h)
+    torch.cuda.synchronize()
+    _no_device_error()
+    r = oracle.denoise_step(dm.as_dict(), wl.layers, wl.phi_table[wl.t - 1], wl.w_lm,
+                            t0.cpu().numpy(), m0.cpu().numpy().astype(bool), wl.gamma, wl.t,
+                            wl.T, h=wl.h)
+    compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                           tokens=wl.tokens.cpu().numpy(), masked=wl.masked.cpu().numpy()),
+                   m0.cpu().numpy(), wl.gamma)
+
+
+def test_denoise_step_embed_path_and_stacked_layers(cuda_device):
+    # small decode-loop shape: embedding path, 3 layers, ragged context, several tiles
+    seed = 21
+    dm = synth.Dims(B=3, S=16, d=256, Hq=8, Hkv=2, D=64, V=2048, Lmax=200, n_layers=3)
+    layers = [synth._layer(seed, l, dm, 1 / 16, 1 / math.sqrt(dm.Hq * dm.D), 1.0, cuda_device)
+              for l in range(dm.n_layers)]
+    w_lm = synth.normal((dm.V, dm.d), 0.2, seed, "w_lm", cuda_device)
+    emb = synth.normal((dm.V + 1, dm.d), 1.0, seed, "emb", cuda_device)
+    pos = synth.normal((dm.S, dm.d), 1.0, seed, "pos", cuda_device)
+    phi = synth.phi_table(16, dm.d, seed, cuda_device)
+    ctx = torch.tensor([200, 64, 13], dtype=torch.int32, device=cuda_device)
+    masked = synth.bernoulli((dm.B, dm.S), 0.6, seed, "m", cuda_device).to(torch.uint8)
+    tokens = torch.where(masked.bool(), torch.full((dm.B, dm.S), dm.V, dtype=torch.int32,
+                                                   device=cuda_device),
+                         synth.integers((dm.B, dm.S), dm.V, seed, "tok", cuda_device))
+    t0, m0 = tokens.clone(), masked.clone()
+    conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[4], 5, 16, 0.8,
+                                                tokens, masked, emb=emb, pos=pos, ctx_len=ctx)
+    torch.cuda.synchronize()
+    _no_device_error()
+    r = oracle.denoise_step(dm.as_dict(), layers, phi[4], w_lm, t0.cpu().numpy(),
+                            m0.cpu().numpy().astype(bool), 0.8, 5, 16, emb=emb, pos=pos,
+                            ctx_len=[200, 64, 13])
+    compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                           tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
+                   m0.cpu().numpy(), 0.8)
+
+
+def test_denoise_step_mid_size(cuda_device):
+    wl = synth.mid_step(cuda_device)
+    dm = wl.dims
+    t0, m0 = wl.tokens.clone(), wl.masked.clone()
+    conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), wl.layers, wl.w_lm,
+                                                wl.phi_table[wl.t - 1], wl.t, wl.T, wl.gamma,
+                                                wl.tokens, wl.masked, h=wl.h)
+    torch.cuda.synchronize()
+    _no_device_error()
+    r = oracle.denoise_step(dm.as_dict(), wl.layers, wl.phi_table[wl.t - 1], wl.w_lm,
+                            t0.cpu().numpy(), m0.cpu().numpy().astype(bool), wl.gamma, wl.t,
+                            wl.T, h=wl.h)
+    rep = compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                                 tokens=wl.tokens.cpu().numpy(), masked=wl.masked.cpu().numpy()),
+                         m0.cpu().numpy(), wl.gamma)
+    frac = float((r["conf"][m0.cpu().numpy().astype(bool)] >= 0.8).mean())
+    print("mid step:", rep, "fraction of masked rows with conf >= 0.8:", frac)
+
+
+# ------------------------------------------------------------------------------ decode loop
+
+def _step_trace_gpu(wl, n_steps):
+    dm = wl.dims
+    tokens = wl.tokens.clone()
+    masked = wl.masked.clone()
+    ws = td.workspace(dm.as_dict(), td.TD_FN_DENOISE_STEP)
+    trace = []
+    for t in range(1, wl.T + 1):
+        conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), wl.layers, wl.w_lm,
+                                                    wl.phi_table[t - 1], t, wl.T, wl.gamma,
+                                                    tokens, masked, emb=wl.emb, pos=wl.pos,
+                                                    ws=ws)
+        trace.append(dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                          tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy(),
+                          n=ncom.cpu().numpy()))
+        if int(done.item()):
+            break
+    return trace
+
+
+def test_decode_loop_full_size_sampled(cuda_device):
+    wl = synth.decode_loop(cuda_device)
+    dm = wl.dims
+    trace = _step_trace_gpu(wl, wl.T)
+    _no_device_error()
+    # the loop entry point reproduces the step-by-step run bit for bit
+    tokens, masked = wl.tokens.clone(), wl.masked.clone()
+    steps = td.td_decode_block(dm.as_dict(), wl.layers, wl.emb, wl.pos, wl.w_lm, wl.phi_table,
+                               wl.T, wl.gamma, tokens, masked)
+    torch.cuda.synchronize()
+    assert steps == len(trace)
+    assert np.array_equal(tokens.cpu().numpy(), trace[-1]["tokens"])
+    assert not masked.any()
+    # invariants over the whole batch
+    prev = np.ones((dm.B, dm.S), bool)
+    for rec in trace:
+        live = prev.any(axis=1)
+        assert (rec["n"][live] >= 1).all()
+        assert not (rec["masked"].astype(bool) & ~prev).any()
+        prev = rec["masked"].astype(bool)
+    # oracle on two sampled sequences, step by step, until an excluded decision
+    seqs = [0, dm.B - 1]
+    sub = [{k: v.cpu() for k, v in L.items()} for L in _oracle_layers(wl, seqs)]
+    w_cpu, emb_cpu, pos_cpu, phi_cpu = wl.w_lm.cpu(), wl.emb.cpu(), wl.pos.cpu(), wl.phi_table.cpu()
+    dsub = dict(dm.as_dict(), B=len(seqs))
+    tok = np.full((len(seqs), dm.S), dm.V)
+    msk = np.ones((len(seqs), dm.S), bool)
+    for t, rec in enumerate(trace, start=1):
+        r = oracle.denoise_step(dsub, sub, phi_cpu[t - 1], w_cpu, tok, msk, wl.gamma,
+                                t, wl.T, emb=emb_cpu, pos=pos_cpu)
+        rep = compare_commit(r, dict(conf=rec["conf"][seqs], pred=rec["pred"][seqs],
+                                     tokens=rec["tokens"][seqs], masked=rec["masked"][seqs]),
+                             msk, wl.gamma)
+        if rep["excluded_sequences"]:
+            print("decode loop: stopped comparing at step", t, rep)
+            break
+        tok, msk = r["tokens"], r["masked"]
+        if not msk.any():
+            break
