@@ -197,6 +197,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["attention", "lmhead"],
+                    help="launch one kernel family alone (for profiler captures)")
+    ap.add_argument("--B", type=int, default=32)
+    ap.add_argument("--L", type=int, default=8192)
+    ap.add_argument("--M", type=int, default=1024)
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
 
     world, rank, local = dist_setup()
@@ -204,6 +210,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.only:
+        run_only(args)
         return
 
     import block_diffusion_lm_denoise_b300 as td
@@ -355,6 +364,34 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_only(args):
+    """One kernel family on one workload, `reps` launches, no timing: the command that the
+    profiler captures (attention: B sequences, context L; lmhead: M rows)."""
+    import block_diffusion_lm_denoise_b300 as td
+    from block_diffusion_lm_denoise_b300 import synth
+    dev = torch.device("cuda", 0)
+    if args.only == "attention":
+        wl = synth.attention_sweep(args.L, dev, B=args.B)
+        lay = wl.layers[0]
+        dims = wl.dims.as_dict()
+        ws = td.workspace(dims, td.TD_FN_BLOCK_ATTENTION, dev)
+        o = torch.empty_like(lay["q"])
+        for _ in range(args.reps):
+            td.td_block_attention(dims, lay["q"], lay["k_blk"], lay["v_blk"], lay["k_ctx"],
+                                  lay["v_ctx"], o=o, ws=ws)
+    else:
+        wl = synth.lmhead_sweep(args.M, 16, 0.8, dev)
+        dims = wl.dims.as_dict()
+        ws = td.workspace(dims, td.TD_FN_LMHEAD_COMMIT, dev)
+        for _ in range(args.reps):
+            wl.tokens.fill_(wl.dims.V)
+            wl.masked.fill_(1)
+            td.td_lmhead_commit(dims, wl.h, wl.w_lm, 0.8, False, wl.tokens, wl.masked, ws=ws)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    print(json.dumps({"only": args.only, "reps": args.reps, "ok": True}))
 
 
 def run_reference(args, world, rank):
