@@ -24,7 +24,8 @@ TD_FN_DECODE_BLOCK = 4
 
 # Every symbol the header declares (checked by the tests).
 EXPORTED = ("td_workspace_size", "td_status_string", "td_adaln_modulate", "td_block_attention",
-            "td_lmhead_commit", "td_denoise_step", "td_decode_block", "td_device_error")
+            "td_lmhead_commit", "td_denoise_step", "td_decode_block", "td_device_error",
+            "td_lmhead_commit_static")
 
 
 class TdError(RuntimeError):
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
                                       vp, vp, vp, i, i, f, vp, vp, vp, vp, vp, vp,
                                       ctypes.POINTER(i), vp, sz, vp]
         L.td_device_error.argtypes = [ctypes.POINTER(i)]
+        L.td_lmhead_commit_static.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, vp, vp, vp,
+                                               vp, vp, vp, vp]
         for name in EXPORTED:
             if name not in ("td_workspace_size", "td_status_string"):
                 getattr(L, name).restype = i
@@ -179,6 +182,21 @@ def td_lmhead_commit(dims, h, w_lm, gamma: float, force_all: bool, tokens, maske
                                   _ptr(tokens), _ptr(masked), _ptr(conf), _ptr(pred),
                                   _ptr(n_committed), _ptr(all_done), _ptr(ws), ws.numel(),
                                   _stream(stream)))
+    return conf, pred, n_committed, all_done
+
+
+def td_lmhead_commit_static(dims, h, w_lm, gamma: float, force_all: bool, tokens, masked,
+                            conf=None, pred=None, n_committed=None, all_done=None, stream=None):
+    """td_lmhead_commit with the library's fixed 16 MiB device scratch instead of a
+    caller workspace (for callers that cannot allocate); calls must not overlap on the GPU."""
+    dm = dims if isinstance(dims, td_dims) else dims_from(dims)
+    conf, pred, n_committed, all_done = _outs(dm.B, dm.S, h.device, conf, pred, n_committed,
+                                              all_done)
+    _check("td_lmhead_commit_static",
+           lib().td_lmhead_commit_static(ctypes.byref(dm), _ptr(h), _ptr(w_lm), gamma,
+                                         int(force_all), _ptr(tokens), _ptr(masked), _ptr(conf),
+                                         _ptr(pred), _ptr(n_committed), _ptr(all_done),
+                                         _stream(stream)))
     return conf, pred, n_committed, all_done
 
 

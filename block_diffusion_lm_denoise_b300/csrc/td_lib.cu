@@ -536,3 +536,56 @@ td_status td_device_error(int* code) {
 }
 
 }  // extern "C"
+
+// ==========================================================================================
+// td_lmhead_commit_static: the LM head + commit with its scratch in a fixed device array,
+// for callers that cannot allocate device memory.
+// ==========================================================================================
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB
+constexpr int kMaxDevices = 64;
+
+// The scratch itself. In host code this name is only a stand-in for the device symbol, never
+// an address a kernel may use: the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_lm_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per device.
+td_status static_scratch_addr(void** out) {
+  int dev = -1;
+  TD_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return TD_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (g_static_addr[dev] == nullptr) {
+    void* p = nullptr;
+    TD_CUDA(cudaGetSymbolAddress(&p, g_lm_static_scratch));
+    if (p == nullptr || (reinterpret_cast<uintptr_t>(p) % kAlign) != 0) return TD_ERR_CUDA;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return TD_OK;
+}
+
+}  // namespace
+
+extern "C" td_status td_lmhead_commit_static(const td_dims* dims, const void* h,
+                                             const void* w_lm, float gamma, int force_all,
+                                             int* tokens, unsigned char* masked, float* conf,
+                                             int* pred, int* n_committed, int* all_done,
+                                             void* stream) {
+  td_status s = check_lm_dims(dims);
+  if (s != TD_OK) return s;
+  if (!h || !w_lm || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
+    return TD_ERR_INVALID_ARG;
+  if (std::isnan(gamma)) return TD_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w_lm)) return TD_ERR_INVALID_ARG;
+  if (lm_ws_bytes(dims->B * dims->S, dims->V) > kStaticScratchBytes) return TD_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if ((s = static_scratch_addr(&ws)) != TD_OK) return s;
+  // run_lmhead_commit clears the commit counters in the scratch before the merge kernel.
+  return run_lmhead_commit(dims, h, w_lm, gamma, force_all, tokens, masked, conf, pred,
+                           n_committed, all_done, ws, (cudaStream_t)stream, sm_count());
+}

@@ -179,6 +179,27 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
  * current device is used. Synchronises the device. Returns TD_ERR_CUDA if the read fails. */
 td_status td_device_error(int* code);
 
+/* td_lmhead_commit without a caller-provided workspace. The pages have no counterpart: this
+ * is a convenience of the library for callers that cannot allocate device memory, such as
+ * a plugin running inside a host framework whose device memory is owned by that framework's
+ * own pool or budget, or a latency-bound loop that must never call cudaMalloc / cudaFree
+ * (both may synchronise the device). Same arguments, semantics and results as
+ * td_lmhead_commit, minus ws / ws_bytes.
+ * Scratch: a fixed 16 MiB array in device memory that is part of this library, so every GPU
+ * that loads the library holds it until the process exits. Its device address is looked up
+ * on the first call made on each device (with that device current); make that first call
+ * before any stream capture. Nothing is allocated, by this call or by that set-up.
+ * Limit: B*S * ceil(V / N_tile) * 12 + 256 bytes must fit in 16 MiB, with N_tile = 128 for
+ * B*S <= 128 and 256 otherwise (e.g. B*S <= 2048 rows at V = 131072); larger problems return
+ * TD_ERR_WORKSPACE with nothing launched.
+ * All calls share the one array and it keeps the last call's contents (the commit counters
+ * are cleared by every call): calls that can overlap on the GPU (different streams, or
+ * different host threads) race on it and must be serialised by the caller. */
+td_status td_lmhead_commit_static(const td_dims* dims, const void* h, const void* w_lm,
+                                  float gamma, int force_all, int* tokens,
+                                  unsigned char* masked, float* conf, int* pred,
+                                  int* n_committed, int* all_done, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
