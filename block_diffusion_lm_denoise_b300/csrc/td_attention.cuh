@@ -11,13 +11,19 @@
 // group writes the normalised bf16 output directly, otherwise it writes an unnormalised
 // partial (O, running max, running sum) that attn_merge_kernel combines by log-sum-exp.
 //
-// Roles (320 threads): warps 0-3 = softmax/epilogue of rows 0-127, warps 4-7 = rows 128-255,
-// warp 8 lane 0 = TMA producer, warp 9 = TMEM allocator + (lane 0) MMA issuer.
-// TMEM (512 columns): O[h] at columns 128h (fp32, D columns), S[h][buf] at 256 + 64(2h+buf).
-// Per tile: S[h] = Q[h] K^T (M=128, N=64, K=D), softmax warps turn S into bf16 P in shared
-// memory (128-byte swizzled K-major rows), then O[h] += P V (M=128, N=D, K=64, V read
-// MN-major straight from the TMA tile). The MMA of S for tile n+1 is issued before the PV
-// MMA of tile n, so the tensor pipe works while the softmax warps compute exponentials.
+// Roles (608 threads): warps 0-7 = softmax/epilogue of rows 0-127 (two warps per 32 rows,
+// one per half of each 64-key tile), warps 8-15 = rows 128-255, warp 16 lane 0 = TMA
+// producer, warps 17-20 lane 0 = MMA issuers: S = Q K^T of rows 0-127 / 128-255 (17, 18)
+// and O += P V of rows 0-127 / 128-255 (19, 20); warp 17 also owns the TMEM allocation.
+// A tcgen05.mma issue costs about a hundred cycles and a tile needs twelve per half, so the
+// issue is spread over four threads; the four streams touch disjoint TMEM columns.
+// TMEM (512 columns): O[h] at columns 128h (fp32, D columns); S[h] at 256 + 64h (fp32, 64
+// keys); P[h][buf] at 384 + 32(2h+buf) (bf16 probabilities, two per column).
+// Per tile n: S[h] = Q[h] K^T (M=128, N=64, K=D); the softmax warps read S and write P into
+// buffer n&1; O[h] += P V is issued with A = P from TMEM and B = V read MN-major straight
+// from the TMA tile. As soon as the softmax warps have read S(n) the MMA warp issues S for
+// tile n+1, which runs on the tensor pipe while they compute exponentials, and P is double
+// buffered, so the softmax warps never wait on the PV of the previous tile.
 // Rescaling of O is lazy: the running max only moves when a tile's max exceeds it by more
 // than 8 (log2 units), so P stays <= 2^8 and the TMEM round trip is rare.
 #pragma once
@@ -41,8 +47,11 @@ struct AttnParams {
   float scale_log2;          // log2(e) / sqrt(D)
 };
 
-constexpr int kAttnStages = 3;
-constexpr int kAttnThreads = 320;
+constexpr int kAttnStages = 4;
+constexpr int kAttnThreads = 672;   // 16 softmax warps + producer + 4 MMA issuers
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;        // first MMA issuer warp; also allocates the TMEM
+// warps 17, 18: S = Q K^T for halves 0, 1; warps 19, 20: O += P V for halves 0, 1
 
 template <int D>
 struct AttnSmem {
@@ -51,13 +60,16 @@ struct AttnSmem {
   static constexpr int kKVHalf = 64 * 128;                    // 64 keys x 64 bf16
   static constexpr int kKBytes = kKVHalf * (D / 64);
   static constexpr int kStageBytes = 2 * kKBytes;             // K then V
-  static constexpr int kPBytes = 128 * 128;                   // 128 rows x 64 bf16, per half
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQBytes;
-  static constexpr int kOffP = kOffKV + kAttnStages * kStageBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffX = kOffKV + kAttnStages * kStageBytes;   // row max / sum exchange
+  static constexpr int kOffBar = kOffX + 8192;
   static constexpr int kBytes = kOffBar + 512 + 1024;
 };
+
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
 
 __device__ __forceinline__ long long attn_lo(long long c, long long total, int ncta) {
   return c * total / ncta;
@@ -104,6 +116,51 @@ __device__ __forceinline__ int attn_seg_work(const AttnParams& p, const SegInfo&
   return n;
 }
 
+// Walks the live tiles of one CTA in order: segment (row group) by segment.
+struct TileCursor {
+  SegInfo s;
+  int grp, t, wi, nwork, sgw;   // sgw: index among segments with work
+  bool valid;
+};
+
+__device__ __forceinline__ void cursor_next_segment(TileCursor& c, const AttnParams& p,
+                                                    long long lo, long long hi, int grp_last) {
+  for (++c.grp; c.grp <= grp_last; ++c.grp) {
+    const SegInfo s = attn_seg(p, lo, hi, c.grp);
+    const int nw = attn_seg_work(p, s);
+    if (nw > 0) {
+      c.s = s;
+      c.nwork = nw;
+      c.wi = 0;
+      ++c.sgw;
+      c.t = s.t0;
+      while (!attn_tile_live(p, s, c.t)) ++c.t;
+      c.valid = true;
+      return;
+    }
+  }
+  c.valid = false;
+}
+
+__device__ __forceinline__ void cursor_init(TileCursor& c, const AttnParams& p, long long lo,
+                                            long long hi, int grp_first, int grp_last) {
+  c.grp = grp_first - 1;
+  c.sgw = -1;
+  c.valid = false;
+  cursor_next_segment(c, p, lo, hi, grp_last);
+}
+
+__device__ __forceinline__ void cursor_next(TileCursor& c, const AttnParams& p, long long lo,
+                                            long long hi, int grp_last) {
+  if (c.valid && c.wi + 1 < c.nwork) {
+    ++c.t;
+    while (!attn_tile_live(p, c.s, c.t)) ++c.t;
+    ++c.wi;
+    return;
+  }
+  cursor_next_segment(c, p, lo, hi, grp_last);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fused_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -117,18 +174,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sKV = smem + L::kOffKV;
-  uint8_t* sP = smem + L::kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-  uint64_t* kv_full = bars;                       // [3]
-  uint64_t* kv_empty = bars + 3;                  // [3]
-  uint64_t* q_full = bars + 6;
-  uint64_t* q_empty = bars + 7;
-  uint64_t* s_full = bars + 8;                    // [h*2 + buf]
-  uint64_t* s_empty = bars + 12;                  // [h*2 + buf]
-  uint64_t* p_full = bars + 16;                   // [h]
-  uint64_t* o_done = bars + 18;                   // [h]
-  uint64_t* o_free = bars + 20;                   // [h]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+  uint64_t* kv_full = bars;                       // [kAttnStages]
+  uint64_t* kv_empty = bars + kAttnStages;        // [kAttnStages]
+  uint64_t* q_full = bars + 2 * kAttnStages;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* s_full = q_full + 2;                  // [h]          S written
+  uint64_t* s_empty = s_full + 2;                 // [h]          S read by the softmax warps
+  uint64_t* p_full = s_empty + 2;                 // [h*2 + buf]  P written
+  uint64_t* o_done = p_full + 4;                  // [h*2 + buf]  PV of a tile using P[buf] done
+  uint64_t* o_free = o_done + 4;                  // [h]          O read out at a segment end
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_free + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -149,22 +205,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAttnStages; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_empty[i], NH);      // one commit per MMA issuer
     }
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 128);
-    }
+    mbar_init(q_empty, NH);
     for (int h = 0; h < 2; ++h) {
-      mbar_init(&p_full[h], 128);
-      mbar_init(&o_done[h], 1);
-      mbar_init(&o_free[h], 128);
+      mbar_init(&s_full[h], 1);
+      mbar_init(&s_empty[h], 256);
+      mbar_init(&o_free[h], 256);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&p_full[i], 256);
+      mbar_init(&o_done[i], 1);
     }
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -173,7 +229,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ================================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -225,100 +281,96 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(128, 64, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, D, 1);
+  } else if (warp >= kMmaWarp && warp < kMmaWarp + 4) {
+    // ================================================================ MMA issuers
+    const int role = warp - kMmaWarp;              // 0, 1: QK of half role; 2, 3: PV of half role-2
+    const int h = role & 1;
+    if (lane == 0 && h < NH) {
+      TileCursor c;
+      cursor_init(c, p, lo, hi, grp_first, grp_last);
+      int n = 0;
       bool ok = true;
-      int n = 0, sgw = 0, issued = 0;
-      // pending PV: the previous work tile
-      int pv_n = -1, pv_st = 0, pv_first = 0, pv_sgw = 0;
-      auto issue_pv = [&](int m, int st, int first, int sg) -> bool {
-        for (int h = 0; h < NH; ++h) {
-          if (!mbar_wait(&p_full[h], m & 1, ERR_WAIT_EPI)) return false;
-          if (first && sg >= 1 && !mbar_wait(&o_free[h], (sg - 1) & 1, ERR_WAIT_EPI)) return false;
-          tc_fence_after();
-          const uint32_t pa = smem_u32(sP + h * L::kPBytes);
-          const uint32_t vb = smem_u32(sKV + st * L::kStageBytes + L::kKBytes);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_bf16_ss(tmem + h * 128, sdesc_sw128(pa + kk * 32, 16, 1024),
-                        sdesc_sw128(vb + kk * 2048, L::kKVHalf, 1024), idesc_pv,
-                        !(first && kk == 0));
-          }
-          mma_commit(&o_done[h]);
-        }
-        mma_commit(&kv_empty[st]);
-        ++issued;
-        return true;
-      };
-      for (int grp = grp_first; grp <= grp_last && ok; ++grp) {
-        const SegInfo s = attn_seg(p, lo, hi, grp);
-        const int nwork = attn_seg_work(p, s);
-        if (nwork == 0) continue;
-        int wi = 0;
-        for (int t = s.t0; t < s.t1 && ok; ++t) {
-          if (!attn_tile_live(p, s, t)) continue;
+      if (role < 2) {
+        // ---------------------------------------------------------- S[h] = Q[h] K^T
+        constexpr uint32_t idesc_qk = idesc_bf16(128, 64, 0);
+        // descriptors of k-step 0; later k-steps add (byte offset >> 4) to the address field
+        const uint64_t qdesc = sdesc_sw128(smem_u32(sQ + h * 128 * 128), 16, 1024);
+        const uint32_t sacc = tmem + 256 + h * 64;
+        for (; c.valid; ++n) {
           const int st = n % kAttnStages;
-          const int first = (wi == 0), last = (wi == nwork - 1);
           if (!mbar_wait(&kv_full[st], (n / kAttnStages) & 1, ERR_WAIT_TMA)) { ok = false; break; }
-          if (first && !mbar_wait(q_full, sgw & 1, ERR_WAIT_TMA)) { ok = false; break; }
+          if (c.wi == 0 && !mbar_wait(q_full, c.sgw & 1, ERR_WAIT_TMA)) { ok = false; break; }
+          if (n >= 1 && !mbar_wait(&s_empty[h], (n - 1) & 1, ERR_WAIT_EPI)) { ok = false; break; }
           tc_fence_after();
-          const int buf = n & 1;
-          for (int h = 0; h < NH; ++h) {
-            if (n >= 2 &&
-                !mbar_wait(&s_empty[h * 2 + buf], ((n >> 1) - 1) & 1, ERR_WAIT_EPI)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sacc = tmem + 256 + (h * 2 + buf) * 64;
-            const uint32_t qa = smem_u32(sQ + h * 128 * 128);
-            const uint32_t kb = smem_u32(sKV + st * L::kStageBytes);
+          const uint64_t kdesc = sdesc_sw128(smem_u32(sKV + st * L::kStageBytes), 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const int kh = kk >> 2, k4 = kk & 3;
-              mma_bf16_ss(sacc, sdesc_sw128(qa + kh * L::kQRegion + k4 * 32, 16, 1024),
-                          sdesc_sw128(kb + kh * L::kKVHalf + k4 * 32, 16, 1024), idesc_qk,
-                          kk != 0);
-            }
-            mma_commit(&s_full[h * 2 + buf]);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t qa = qdesc + (((kk >> 2) * L::kQRegion + (kk & 3) * 32) >> 4);
+            const uint64_t kb = kdesc + (((kk >> 2) * L::kKVHalf + (kk & 3) * 32) >> 4);
+            mma_bf16_ss(sacc, qa, kb, idesc_qk, kk != 0);
           }
-          if (!ok) break;
-          if (last) mma_commit(q_empty);
-          if (pv_n >= 0 && !issue_pv(pv_n, pv_st, pv_first, pv_sgw)) { ok = false; break; }
-          pv_n = n; pv_st = st; pv_first = first; pv_sgw = sgw;
-          ++n;
-          ++wi;
+          mma_commit(&s_full[h]);
+          if (c.wi == c.nwork - 1) mma_commit(q_empty);
+          cursor_next(c, p, lo, hi, grp_last);
         }
-        ++sgw;
+        // Let every MMA issued so far finish before the TMEM is released.
+        if (n > 0) mbar_wait(&s_full[h], (n - 1) & 1, ERR_WAIT_MMA);
+      } else {
+        // ---------------------------------------------------------- O[h] += P[h] V
+        constexpr uint32_t idesc_pv = idesc_bf16(128, D, 1);
+        for (; c.valid; ++n) {
+          const int st = n % kAttnStages;
+          const int buf = n & 1;
+          const bool first = c.wi == 0;
+          if (!mbar_wait(&p_full[h * 2 + buf], (n >> 1) & 1, ERR_WAIT_EPI)) { ok = false; break; }
+          if (first && c.sgw >= 1 && !mbar_wait(&o_free[h], (c.sgw - 1) & 1, ERR_WAIT_EPI)) {
+            ok = false;
+            break;
+          }
+          // V of this stage: complete (the S of this tile, computed from the same stage, was
+          // read before P existed); waiting also makes the TMA writes visible to this thread
+          if (!mbar_wait(&kv_full[st], (n / kAttnStages) & 1, ERR_WAIT_TMA)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t vdesc =
+              sdesc_sw128(smem_u32(sKV + st * L::kStageBytes + L::kKBytes), L::kKVHalf, 1024);
+          const uint32_t pa = tmem + 384 + (h * 2 + buf) * 32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(tmem + h * 128, pa + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_pv,
+                        !(first && kk == 0));
+          mma_commit(&o_done[h * 2 + buf]);
+          mma_commit(&kv_empty[st]);
+          cursor_next(c, p, lo, hi, grp_last);
+        }
+        if (n > 0) mbar_wait(&o_done[h * 2 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, ERR_WAIT_MMA);
       }
-      if (ok && pv_n >= 0) ok = issue_pv(pv_n, pv_st, pv_first, pv_sgw);
-      // Let every MMA issued so far finish before the TMEM is released.
-      if (n > 0) {
-        const int j = n - 1;
-        mbar_wait(&s_full[(0 * 2) + (j & 1)], (j >> 1) & 1, ERR_WAIT_MMA);
-      }
-      if (issued > 0) {
-        const int j = issued - 1;
-        for (int h = 0; h < NH; ++h) mbar_wait(&o_done[h], j & 1, ERR_WAIT_MMA);
-      }
+      (void)ok;
     }
     __syncwarp();
   } else {
     // ================================================================ softmax / epilogue
-    const int h = warp >> 2;              // MMA half
-    const int q4 = warp & 3;              // TMEM lane quarter
-    const int r = h * 128 + q4 * 32 + lane;
+    // Warp w: MMA half h = w / 8, column half c = (w / 4) % 2 (keys 32c..32c+31 of every
+    // tile, O columns c*D/2 ..), TMEM lane quarter q4 = w % 4. The two warps (h, 0, q4) and
+    // (h, 1, q4) own the same 32 rows: they agree on the row maximum through shared memory and
+    // named barrier 1 + 4h + q4, and add their partial row sums at the end of a segment.
+    // A wait that runs out records the error and the loop carries on, so both warps of a
+    // pair always meet at the same barriers.
+    const int h = warp >> 3;
+    const int c = (warp >> 2) & 1;
+    const int q4 = warp & 3;
+    const int rr = q4 * 32 + lane;
+    const int r = h * 128 + rr;
     const bool row_ok = r < p.R;
     const bool half_live = h < NH;
+    const int bar_id = 1 + h * 4 + q4;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    constexpr int DH = D / 2;
+    float* xmax = reinterpret_cast<float*>(smem + L::kOffX);   // [buf][h][c][128]
+    float* xl = xmax + 2 * 2 * 2 * 128;                         // [h][c][128]
     const float sc = p.scale_log2;
     int n = 0;
-    bool ok = true;
     float m_run = -INFINITY, l_run = 0.f;
-    for (int grp = grp_first; grp <= grp_last && ok; ++grp) {
+    for (int grp = grp_first; grp <= grp_last; ++grp) {
       const SegInfo s = attn_seg(p, lo, hi, grp);
       const int nwork = attn_seg_work(p, s);
       const int s_tok = r / p.Gc;
@@ -326,40 +378,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int rec = blockIdx.x * p.max_seg + (grp - grp_first);
       if (nwork == 0 || !half_live) {
         // No key reaches this segment (or this half has no rows): an empty partial.
-        if (half_live && row_ok && !s.full) {
+        if (half_live && c == 0 && row_ok && !s.full) {
           p.part_ml[((size_t)rec * p.R + r) * 2 + 0] = -INFINITY;
           p.part_ml[((size_t)rec * p.R + r) * 2 + 1] = 0.f;
         }
-        if (nwork != 0) n += nwork;
+        n += nwork;
         continue;
       }
       int wi = 0;
-      for (int t = s.t0; t < s.t1 && ok; ++t) {
+      for (int t = s.t0; t < s.t1; ++t) {
         if (!attn_tile_live(p, s, t)) continue;
-        const int first = (wi == 0), last = (wi == nwork - 1);
+        const bool first = (wi == 0), last = (wi == nwork - 1);
         const int buf = n & 1;
-        if (!mbar_wait(&s_full[h * 2 + buf], (n >> 1) & 1, ERR_WAIT_MMA)) { ok = false; break; }
+        mbar_wait(&s_full[h], n & 1, ERR_WAIT_MMA);
         tc_fence_after();
-        float x[64];
-        {
-          float a[32], b2[32];
-          const uint32_t sacc = tmem + lane_off + 256 + (h * 2 + buf) * 64;
-          tmem_ld32(sacc, a);
-          tmem_ld32(sacc + 32, b2);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) { x[j] = a[j]; x[32 + j] = b2[j]; }
-        }
+        float x[32];
+        tmem_ld32(tmem + lane_off + 256 + h * 64 + c * 32, x);
+        tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&s_empty[h * 2 + buf]);
+        mbar_arrive(&s_empty[h]);
         const int nvalid = (t < p.n_ctx_tiles) ? min(64, s.L - t * 64) : p.S;
-        float tmax = -INFINITY;
+        if (nvalid < 64) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          x[j] = (j < nvalid) ? x[j] * sc : -INFINITY;
-          tmax = fmaxf(tmax, x[j]);
+          for (int j = 0; j < 32; ++j)
+            if (c * 32 + j >= nvalid) x[j] = -INFINITY;
         }
-        bool waited = false;
+        // row maximum of the raw scores (8 independent chains), then the partner's half;
+        // scaling by log2(e)/sqrt(D) > 0 commutes with the maximum
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+        for (int j = 8; j < 32; ++j) mx[j & 7] = fmaxf(mx[j & 7], x[j]);
+        const float pm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        float* xb = xmax + (buf * 2 + h) * 2 * 128;
+        xb[c * 128 + rr] = pm;
+        pair_sync(bar_id);
+        const float tmax = fmaxf(xb[rr], xb[128 + rr]) * sc;
         if (first) {
           m_run = tmax;
           l_run = 0.f;
@@ -367,63 +423,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float alpha = ex2_approx(m_run - tmax);
           m_run = tmax;
           l_run *= alpha;
-          if (!mbar_wait(&o_done[h], (n - 1) & 1, ERR_WAIT_MMA)) { ok = false; break; }
-          waited = true;
+          // every PV so far (the last one used P[(n-1)&1]) must be done before O is touched
+          mbar_wait(&o_done[h * 2 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, ERR_WAIT_MMA);
           tc_fence_after();
-          const uint32_t oacc = tmem + lane_off + h * 128;
+          const uint32_t oacc = tmem + lane_off + h * 128 + c * DH;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int k = 0; k < DH / 32; ++k) {
             float o[32];
-            tmem_ld32(oacc + c * 32, o);
+            tmem_ld32(oacc + k * 32, o);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] *= alpha;
-            tmem_st32(oacc + c * 32, o);
+            tmem_st32(oacc + k * 32, o);
           }
-          tmem_st_wait();
         }
-        // P = 2^(x - m) rounded to bf16; the row sum adds the rounded values
-        uint32_t pk[32];
-        float lsum = 0.f;
+        // P = 2^(x*scale - m) rounded to bf16, two per TMEM column (keys 32c.. -> columns
+        // 16c..16c+15 of P[buf]); the running sum adds the fp32 values
+        const float mneg = -m_run;
+        uint32_t pk[16];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float e0 = ex2_approx(x[2 * j] - m_run);
-          const float e1 = ex2_approx(x[2 * j + 1] - m_run);
+        for (int j = 0; j < 16; ++j) {
+          const float e0 = ex2_approx(fmaf(x[2 * j], sc, mneg));
+          const float e1 = ex2_approx(fmaf(x[2 * j + 1], sc, mneg));
           pk[j] = pack_bf16x2(e0, e1);
-          lsum += bf16lo_to_f32(pk[j]) + bf16hi_to_f32(pk[j]);
+          ls[j & 3] += e0 + e1;
         }
-        l_run += lsum;
-        if (n >= 1 && !waited && !mbar_wait(&o_done[h], (n - 1) & 1, ERR_WAIT_MMA)) {
-          ok = false;
-          break;
-        }
-        {
-          // row r of this half: 128 bytes, eight 16-byte chunks XOR-swizzled by (row & 7)
-          const int rr = q4 * 32 + lane;
-          uint8_t* prow = sP + h * L::kPBytes + rr * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 w = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            *reinterpret_cast<uint4*>(prow + ((c ^ (rr & 7)) << 4)) = w;
-          }
-        }
-        fence_proxy_async_smem();
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // P[buf] was last read by the PV of tile n-2
+        if (n >= 2) mbar_wait(&o_done[h * 2 + buf], ((n - 2) >> 1) & 1, ERR_WAIT_MMA);
+        tc_fence_after();
+        tmem_st16(tmem + lane_off + 384 + (h * 2 + buf) * 32 + c * 16, pk);
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&p_full[h]);
+        mbar_arrive(&p_full[h * 2 + buf]);
         if (last) {
-          if (!mbar_wait(&o_done[h], n & 1, ERR_WAIT_MMA)) { ok = false; break; }
+          mbar_wait(&o_done[h * 2 + buf], (n >> 1) & 1, ERR_WAIT_MMA);
           tc_fence_after();
-          const uint32_t oacc = tmem + lane_off + h * 128;
+          // total row sum, added in the same order by both warps of the pair
+          xl[(h * 2 + c) * 128 + rr] = l_run;
+          pair_sync(bar_id);
+          const float ltot = xl[(h * 2) * 128 + rr] + xl[(h * 2 + 1) * 128 + rr];
+          const uint32_t oacc = tmem + lane_off + h * 128 + c * DH;
           if (s.full) {
-            const float inv = 1.f / l_run;
-            uint16_t* dst = p.out + (((size_t)s.b * p.S + s_tok) * p.Hq + head) * D;
+            const float inv = 1.f / ltot;
+            uint16_t* dst = p.out + (((size_t)s.b * p.S + s_tok) * p.Hq + head) * D + c * DH;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int k = 0; k < DH / 32; ++k) {
               float o[32];
-              tmem_ld32(oacc + c * 32, o);
+              tmem_ld32(oacc + k * 32, o);
               tmem_ld_wait();
               if (row_ok) {
-                uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+                uint4* d4 = reinterpret_cast<uint4*>(dst + k * 32);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                   d4[j] = make_uint4(pack_bf16x2(o[8 * j] * inv, o[8 * j + 1] * inv),
@@ -432,26 +483,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                      pack_bf16x2(o[8 * j + 6] * inv, o[8 * j + 7] * inv));
               }
             }
-            if (row_ok && p.lse)
+            if (row_ok && c == 0 && p.lse)
               p.lse[((size_t)s.b * p.S + s_tok) * p.Hq + head] =
-                  (m_run + __log2f(l_run)) * 0.6931471805599453f;
+                  (m_run + __log2f(ltot)) * 0.6931471805599453f;
           } else {
-            float* dst = p.part_o + ((size_t)rec * p.R + r) * D;
+            float* dst = p.part_o + ((size_t)rec * p.R + r) * D + c * DH;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int k = 0; k < DH / 32; ++k) {
               float o[32];
-              tmem_ld32(oacc + c * 32, o);
+              tmem_ld32(oacc + k * 32, o);
               tmem_ld_wait();
               if (row_ok) {
-                float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+                float4* d4 = reinterpret_cast<float4*>(dst + k * 32);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                   d4[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
               }
             }
-            if (row_ok) {
+            if (row_ok && c == 0) {
               p.part_ml[((size_t)rec * p.R + r) * 2 + 0] = m_run;
-              p.part_ml[((size_t)rec * p.R + r) * 2 + 1] = l_run;
+              p.part_ml[((size_t)rec * p.R + r) * 2 + 1] = ltot;
             }
           }
           tc_fence_before();
@@ -465,7 +516,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
