@@ -116,29 +116,37 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // Attention plan
 // ------------------------------------------------------------------------------------------
 struct AttnPlan {
-  int G, Gc, NC, R, n_ctx_tiles, T, n_groups, ncta, max_seg;
+  int G, Gc, NC, R, n_ctx_tiles, T, n_units, n_teams, ncta, max_seg;
   long long total;
   size_t part_o_bytes, part_ml_bytes;
 };
 
+// Teams of NC CTAs (one per 128-row chunk of a (sequence, KV head) unit) share one key range.
+// If the units split evenly over at least 85% of the possible teams, each team takes whole
+// units and no merge pass is needed; otherwise the (unit, tile) space is cut into one equal
+// range per team (split-K) and the partials are merged.
 AttnPlan plan_attention(const td_dims* dm, int nsm) {
   AttnPlan a{};
   a.G = dm->Hq / dm->Hkv;
   a.Gc = 1;
   for (int c = a.G; c >= 1; --c)
-    if (a.G % c == 0 && dm->S * c <= 256) { a.Gc = c; break; }
+    if (a.G % c == 0 && dm->S * c <= 128) { a.Gc = c; break; }
   a.NC = a.G / a.Gc;
   a.R = dm->S * a.Gc;
-  a.n_ctx_tiles = (dm->Lmax + 63) / 64;
+  a.n_ctx_tiles = (dm->Lmax + kKeyTile - 1) / kKeyTile;
   a.T = a.n_ctx_tiles + 1;
-  a.n_groups = dm->B * dm->Hkv * a.NC;
-  a.total = (long long)a.n_groups * a.T;
-  if (a.n_groups <= nsm && a.n_groups * 5 >= nsm * 4)
-    a.ncta = a.n_groups;                       // one CTA per row group: no merge pass
+  a.n_units = dm->B * dm->Hkv;
+  a.total = (long long)a.n_units * a.T;
+  const int max_teams = std::max(1, nsm / a.NC);
+  const int per = (a.n_units + max_teams - 1) / max_teams;
+  const int even = (a.n_units + per - 1) / per;
+  if (a.n_units % per == 0 && even * 100 >= max_teams * 85)
+    a.n_teams = even;
   else
-    a.ncta = (int)std::min<long long>(nsm, a.total);
-  const long long per = (a.total + a.ncta - 1) / a.ncta;
-  a.max_seg = (int)((per + a.T - 1) / a.T) + 1;
+    a.n_teams = (int)std::min<long long>(max_teams, a.total);
+  a.ncta = a.n_teams * a.NC;
+  const long long tiles = (a.total + a.n_teams - 1) / a.n_teams;
+  a.max_seg = (int)((tiles + a.T - 1) / a.T) + 1;
   const size_t recs = (size_t)a.ncta * a.max_seg;
   a.part_o_bytes = align_up(recs * a.R * dm->D * sizeof(float));
   a.part_ml_bytes = align_up(recs * a.R * 2 * sizeof(float));
@@ -252,7 +260,7 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)(empty ? 1 : dm->Lmax),
                               (uint64_t)(empty ? 1 : dm->B * dm->Hkv)};
     const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)(empty ? 1 : dm->Lmax) * D * 2};
-    const uint32_t box[3] = {64, 64, 1};
+    const uint32_t box[3] = {64, (uint32_t)kKeyTile, 1};
     const void* kb = empty ? k_blk : k_ctx;
     const void* vb = empty ? v_blk : v_ctx;
     if (!make_map(&mkc, kb, 3, dims, str, box) || !make_map(&mvc, vb, 3, dims, str, box))
@@ -261,9 +269,11 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
   AttnParams p{};
   p.B = dm->B; p.S = dm->S; p.Hq = dm->Hq; p.Hkv = dm->Hkv; p.D = D; p.Lmax = dm->Lmax;
   p.G = a.G; p.Gc = a.Gc; p.NC = a.NC; p.R = a.R;
-  p.n_ctx_tiles = a.n_ctx_tiles; p.T = a.T; p.n_groups = a.n_groups; p.total = a.total;
+  p.n_ctx_tiles = a.n_ctx_tiles; p.T = a.T; p.n_units = a.n_units; p.n_teams = a.n_teams;
+  p.total = a.total;
   p.max_seg = a.max_seg;
   p.ctx_len = ctx_len;
+  p.q = static_cast<const uint16_t*>(q);
   p.part_o = static_cast<float*>(ws);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + a.part_o_bytes);
   p.out = static_cast<uint16_t*>(o);
@@ -279,8 +289,8 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
                                                                              mvb, p);
   }
   TD_CUDA(cudaGetLastError());
-  if (!(a.n_groups == a.ncta)) {
-    attn_merge_kernel<<<a.n_groups, 256, 0, st>>>(p, a.ncta);
+  if (a.n_teams != a.n_units) {
+    attn_merge_kernel<<<a.n_units * a.NC, 256, 0, st>>>(p);
     TD_CUDA(cudaGetLastError());
   }
   return TD_OK;

@@ -61,6 +61,8 @@ ATTN_CASES = [
     (2, 4, 8, 8, 64, 130, None),              # MHA, tiny block
     (1, 32, 32, 2, 128, 190, None),           # S*G = 512 > 256: two row groups per KV head
     (1, 1, 4, 1, 64, 0, None),                # one key: output == v exactly
+    (3, 16, 32, 2, 128, 4000, [4000, 1234, 0]),  # split-K: several tiles and units per team
+    (4, 16, 16, 4, 64, 2000, None),           # D = 64 with split-K and four KV heads
 ]
 
 
