@@ -50,6 +50,7 @@ struct AttnParams {
   uint16_t* out;             // [B, S, Hq, D] bf16
   float* lse;                // [B, S, Hq] or null
   float scale_log2;          // log2(e) / sqrt(D)
+  const int* skip;           // when non-null and nonzero, return at once
 };
 
 constexpr int kKSlots = 3;         // K ring (a slot is freed when S of its tile is done)
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                       const __grid_constant__ CUtensorMap tmKb,
                       const __grid_constant__ CUtensorMap tmVb, const AttnParams p) {
   using L = AttnSmem<D>;
+  if (p.skip != nullptr && *p.skip != 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -543,6 +545,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // Log-sum-exp merge of the partials of every (unit, row chunk) that no single team covered.
 // One CTA per (unit, chunk); thread (row, 4 columns).
 __global__ void attn_merge_kernel(const AttnParams p) {
+  if (p.skip != nullptr && *p.skip != 0) return;
   const int unit = blockIdx.x / p.NC;
   const int chunk = blockIdx.x % p.NC;
   const long long first_tile = (long long)unit * p.T;

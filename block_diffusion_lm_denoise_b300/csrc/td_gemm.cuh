@@ -35,6 +35,8 @@ struct GemmParams {
   float* part_max;
   int* part_arg;
   float* part_sum;
+  // when non-null and nonzero, the kernel returns at once (a finished decode loop)
+  const int* skip;
 };
 
 template <int BN, int STAGES>
@@ -51,6 +53,7 @@ __global__ void __launch_bounds__(256, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
   using L = GemmSmem<BN, STAGES>;
+  if (p.skip != nullptr && *p.skip != 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));

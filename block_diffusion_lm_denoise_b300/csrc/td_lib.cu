@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <vector>
 
@@ -81,9 +82,25 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
+// Dynamic shared-memory opt-in, done once per (kernel, device) so that no attribute call is
+// made while a decode loop is being captured into a CUDA graph.
+cudaError_t set_smem_raw(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  int& have = done[std::make_pair(kernel, dev)];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return set_smem_raw(reinterpret_cast<const void*>(kernel), bytes);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -205,10 +222,43 @@ td_status gemm_dispatch(const void* A, const void* Bm, int M, int N, int K, Gemm
   return launch_gemm<256, 4, EPI>(A, Bm, M, N, K, gp, st, nsm);
 }
 
+template <int NK>
+td_status launch_adaln_nk(const void* h, const float* E, const float* phi, int rows, int d,
+                          float eps, void* x_mod, float* gate, cudaStream_t st, const int* skip) {
+  const int smem = 2 * d * (int)sizeof(float);
+  TD_CUDA(set_smem(adaln_modulate_kernel<NK>, smem));
+  adaln_modulate_kernel<NK><<<(rows + kAdaRows - 1) / kAdaRows, kAdaThreads, smem, st>>>(
+      static_cast<const uint16_t*>(h), E, phi, rows, d, eps, static_cast<uint16_t*>(x_mod), gate,
+      skip);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
+}
+
+// adaLN-single modulation: the register path for d = 256 * NK (NK <= 32), else generic.
+td_status launch_adaln(const void* h, const float* E, const float* phi, int rows, int d,
+                       float eps, void* x_mod, float* gate, cudaStream_t st,
+                       const int* skip = nullptr) {
+  switch (d % 256 == 0 ? d / 256 : 0) {
+    case 1: return launch_adaln_nk<1>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
+    case 2: return launch_adaln_nk<2>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
+    case 4: return launch_adaln_nk<4>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
+    case 8: return launch_adaln_nk<8>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
+    case 16: return launch_adaln_nk<16>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
+    case 32: return launch_adaln_nk<32>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
+    default: break;
+  }
+  adaln_modulate_generic_kernel<<<rows, 256, 0, st>>>(static_cast<const uint16_t*>(h), E, phi,
+                                                      d, eps, static_cast<uint16_t*>(x_mod),
+                                                      gate, skip);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
+}
+
 td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, float gamma,
                             int force_all, int* tokens, unsigned char* masked, float* conf,
                             int* pred, int* n_committed, int* all_done, void* ws,
-                            cudaStream_t st, int nsm) {
+                            cudaStream_t st, int nsm, const int* skip = nullptr,
+                            int* steps = nullptr) {
   const int M = dm->B * dm->S;
   const int V = dm->V;
   const int bn = lm_bn(M);
@@ -223,19 +273,22 @@ td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, 
   gp.part_max = pmax;
   gp.part_arg = parg;
   gp.part_sum = psum;
+  gp.skip = skip;
   td_status s = gemm_dispatch<EPI_LMHEAD>(h, w_lm, M, V, dm->d, gp, st, nsm, bn);
   if (s != TD_OK) return s;
   TD_CUDA(cudaMemsetAsync(counters, 0, 2 * sizeof(int), st));
-  merge_commit_kernel<<<dm->B, kCommitThreads, 0, st>>>(pmax, parg, psum, nt, dm->S, gamma,
+  merge_commit_kernel<<<dm->B, 32 * std::min(dm->S, 32), 0, st>>>(pmax, parg, psum, nt, dm->S, gamma,
                                                          force_all, tokens, masked, conf, pred,
-                                                         n_committed, all_done, counters);
+                                                         n_committed, all_done, counters,
+                                                         skip, steps);
   TD_CUDA(cudaGetLastError());
   return TD_OK;
 }
 
 td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, const void* v_blk,
                         const void* k_ctx, const void* v_ctx, const int* ctx_len, void* o,
-                        float* lse, void* ws, cudaStream_t st, int nsm) {
+                        float* lse, void* ws, cudaStream_t st, int nsm,
+                        const int* skip = nullptr) {
   const AttnPlan a = plan_attention(dm, nsm);
   const int D = dm->D;
   CUtensorMap mq, mkc, mvc, mkb, mvb;
@@ -274,6 +327,7 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
   p.max_seg = a.max_seg;
   p.ctx_len = ctx_len;
   p.q = static_cast<const uint16_t*>(q);
+  p.skip = skip;
   p.part_o = static_cast<float*>(ws);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + a.part_o_bytes);
   p.out = static_cast<uint16_t*>(o);
@@ -304,6 +358,7 @@ struct StepWs {
   float* gate;
   void* attn;
   void* lm;
+  int* loop;      // decode-loop step counter
   size_t total;
 };
 
@@ -322,6 +377,7 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
   const size_t o_g = take((size_t)dm->d * 4);
   const size_t o_a = take(attn_ws_bytes(dm, nsm));
   const size_t o_l = take(lm_ws_bytes((int)M, dm->V));
+  const size_t o_c = take(64);
   w.total = off;
   if (base) {
     uint8_t* b = static_cast<uint8_t*>(base);
@@ -334,6 +390,7 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
     w.gate = reinterpret_cast<float*>(b + o_g);
     w.attn = b + o_a;
     w.lm = b + o_l;
+    w.loop = reinterpret_cast<int*>(b + o_c);
   }
   return w;
 }
@@ -342,13 +399,14 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
                    const void* emb, const void* pos, const void* w_lm, const float* phi_t,
                    int t, int T, float gamma, int* tokens, unsigned char* masked, float* conf,
                    int* pred, int* n_committed, int* all_done, void* ws, cudaStream_t st,
-                   int nsm) {
+                   int nsm, const int* skip = nullptr, int* steps = nullptr) {
   const StepWs w = carve_step(dm, ws, nsm);
   const int M = dm->B * dm->S;
   const int d = dm->d;
   if (h == nullptr) {
     embed_kernel<<<M, 256, 0, st>>>(tokens, static_cast<const uint16_t*>(emb),
-                                    static_cast<const uint16_t*>(pos), w.h, dm->S, d, dm->V);
+                                    static_cast<const uint16_t*>(pos), w.h, dm->S, d, dm->V,
+                                    skip);
   } else {
     TD_CUDA(cudaMemcpyAsync(w.h, h, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st));
   }
@@ -357,23 +415,22 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
   const int bn = M >= 512 ? 256 : 128;
   for (int l = 0; l < dm->n_layers; ++l) {
     const td_layer& L = layers[l];
-    adaln_modulate_kernel<<<M, kAdaThreads, 0, st>>>(w.h, L.ada_E, phi_t, d, kLnEps, w.xmod,
-                                                     w.gate);
-    TD_CUDA(cudaGetLastError());
+    td_status sa = launch_adaln(w.h, L.ada_E, phi_t, M, d, kLnEps, w.xmod, w.gate, st, skip);
+    if (sa != TD_OK) return sa;
     GemmParams g1{};
-    g1.q = w.q; g1.k = w.k; g1.v = w.v; g1.nq = nq; g1.nk = nk;
+    g1.q = w.q; g1.k = w.k; g1.v = w.v; g1.nq = nq; g1.nk = nk; g1.skip = skip;
     td_status s = gemm_dispatch<EPI_QKV>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn);
     if (s != TD_OK) return s;
     s = run_attention(dm, w.q, w.k, w.v, L.k_ctx, L.v_ctx, ctx_len, w.o, nullptr, w.attn, st,
-                      nsm);
+                      nsm, skip);
     if (s != TD_OK) return s;
     GemmParams g2{};
-    g2.h = w.h; g2.gate = w.gate;
+    g2.h = w.h; g2.gate = w.gate; g2.skip = skip;
     s = gemm_dispatch<EPI_RESID>(w.o, L.wo, M, d, nq, g2, st, nsm, bn);
     if (s != TD_OK) return s;
   }
   return run_lmhead_commit(dm, w.h, w_lm, gamma, t == T ? 1 : 0, tokens, masked, conf, pred,
-                           n_committed, all_done, w.lm, st, nsm);
+                           n_committed, all_done, w.lm, st, nsm, skip, steps);
 }
 
 td_status check_layers(const td_dims* dm, const td_layer* layers) {
@@ -386,6 +443,135 @@ td_status check_layers(const td_dims* dm, const td_layer* layers) {
         (dm->Lmax > 0 && (!aligned16(L.k_ctx) || !aligned16(L.v_ctx))))
       return TD_ERR_INVALID_ARG;
   }
+  return TD_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// Decode loop as one CUDA graph: the T steps are captured once per distinct argument set (on
+// a private stream, since the legacy default stream cannot be captured) and replayed on the
+// caller's stream. Every kernel of step t+1 reads the all-done word that step t's commit
+// wrote and returns at once when it is set; merge_commit counts the steps that ran.
+// ------------------------------------------------------------------------------------------
+void set_all_smem() {
+  set_smem(gemm_tn_kernel<128, 6, EPI_QKV>, GemmSmem<128, 6>::kBytes);
+  set_smem(gemm_tn_kernel<128, 6, EPI_RESID>, GemmSmem<128, 6>::kBytes);
+  set_smem(gemm_tn_kernel<128, 6, EPI_LMHEAD>, GemmSmem<128, 6>::kBytes);
+  set_smem(gemm_tn_kernel<256, 4, EPI_QKV>, GemmSmem<256, 4>::kBytes);
+  set_smem(gemm_tn_kernel<256, 4, EPI_RESID>, GemmSmem<256, 4>::kBytes);
+  set_smem(gemm_tn_kernel<256, 4, EPI_LMHEAD>, GemmSmem<256, 4>::kBytes);
+  set_smem(attn_fused_kernel<128>, AttnSmem<128>::kBytes);
+  set_smem(attn_fused_kernel<64>, AttnSmem<64>::kBytes);
+  set_smem(adaln_modulate_kernel<1>, 2 * 256 * 1 * 4);
+  set_smem(adaln_modulate_kernel<2>, 2 * 256 * 2 * 4);
+  set_smem(adaln_modulate_kernel<4>, 2 * 256 * 4 * 4);
+  set_smem(adaln_modulate_kernel<8>, 2 * 256 * 8 * 4);
+  set_smem(adaln_modulate_kernel<16>, 2 * 256 * 16 * 4);
+  set_smem(adaln_modulate_kernel<32>, 2 * 256 * 32 * 4);
+}
+
+struct LoopKey {
+  std::vector<uint64_t> v;
+  bool operator<(const LoopKey& o) const { return v < o.v; }
+};
+
+std::mutex g_loop_mu;
+std::map<LoopKey, cudaGraphExec_t> g_loop_graphs;
+std::vector<LoopKey> g_loop_order;
+constexpr size_t kMaxLoopGraphs = 16;
+
+cudaStream_t capture_stream() {
+  static std::mutex mu;
+  static std::map<int, cudaStream_t> streams;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = streams.find(dev);
+  if (it != streams.end()) return it->second;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+  streams[dev] = s;
+  return s;
+}
+
+// Runs the loop through a cached graph. TD_ERR_UNSUPPORTED means "capture not possible here":
+// the caller then runs the host loop.
+td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx_len,
+                       const void* emb, const void* pos, const void* w_lm,
+                       const float* phi_table, int t_start, int T, float gamma, int* tokens,
+                       unsigned char* masked, float* conf, int* pred, int* n_committed,
+                       int* all_done, void* ws, size_t ws_bytes, cudaStream_t st, int nsm,
+                       int* steps_taken, int* done) {
+  const StepWs w = carve_step(dm, ws, nsm);
+  LoopKey key;
+  int dev = 0;
+  TD_CUDA(cudaGetDevice(&dev));
+  auto u = [&](const void* p) { key.v.push_back(reinterpret_cast<uintptr_t>(p)); };
+  key.v = {(uint64_t)dev, (uint64_t)dm->B, (uint64_t)dm->S, (uint64_t)dm->d, (uint64_t)dm->Hq,
+           (uint64_t)dm->Hkv, (uint64_t)dm->D, (uint64_t)dm->V, (uint64_t)dm->Lmax,
+           (uint64_t)dm->n_layers, (uint64_t)t_start, (uint64_t)T, (uint64_t)ws_bytes};
+  uint32_t gbits;
+  std::memcpy(&gbits, &gamma, 4);
+  key.v.push_back(gbits);
+  for (int l = 0; l < dm->n_layers; ++l) {
+    u(layers[l].wqkv); u(layers[l].wo); u(layers[l].ada_E); u(layers[l].k_ctx); u(layers[l].v_ctx);
+  }
+  u(ctx_len); u(emb); u(pos); u(w_lm); u(phi_table); u(tokens); u(masked); u(conf); u(pred);
+  u(n_committed); u(all_done); u(ws);
+  cudaGraphExec_t exec = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_loop_mu);
+    auto it = g_loop_graphs.find(key);
+    if (it != g_loop_graphs.end()) exec = it->second;
+  }
+  if (exec == nullptr) {
+    set_all_smem();
+    cudaStream_t cs = capture_stream();
+    if (cs == nullptr) return TD_ERR_UNSUPPORTED;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      cudaGetLastError();
+      return TD_ERR_UNSUPPORTED;
+    }
+    td_status s = TD_OK;
+    if (cudaMemsetAsync(all_done, 0, sizeof(int), cs) != cudaSuccess ||
+        cudaMemsetAsync(w.loop, 0, sizeof(int), cs) != cudaSuccess)
+      s = TD_ERR_CUDA;
+    for (int t = t_start; t <= T && s == TD_OK; ++t)
+      s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
+                   phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, tokens, masked, conf,
+                   pred, n_committed, all_done, ws, cs, nsm, all_done, w.loop);
+    cudaGraph_t g = nullptr;
+    const cudaError_t ee = cudaStreamEndCapture(cs, &g);
+    if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
+      if (g) cudaGraphDestroy(g);
+      cudaGetLastError();
+      return s != TD_OK ? s : TD_ERR_UNSUPPORTED;
+    }
+    const cudaError_t ie = cudaGraphInstantiate(&exec, g, 0);
+    cudaGraphDestroy(g);
+    if (ie != cudaSuccess) {
+      cudaGetLastError();
+      return TD_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lk(g_loop_mu);
+    g_loop_graphs[key] = exec;
+    g_loop_order.push_back(key);
+    if (g_loop_order.size() > kMaxLoopGraphs) {
+      auto old = g_loop_graphs.find(g_loop_order.front());
+      if (old != g_loop_graphs.end()) {
+        cudaDeviceSynchronize();
+        cudaGraphExecDestroy(old->second);
+        g_loop_graphs.erase(old);
+      }
+      g_loop_order.erase(g_loop_order.begin());
+    }
+  }
+  TD_CUDA(cudaGraphLaunch(exec, st));
+  int host[2] = {0, 0};
+  TD_CUDA(cudaMemcpyAsync(&host[0], w.loop, sizeof(int), cudaMemcpyDeviceToHost, st));
+  TD_CUDA(cudaMemcpyAsync(&host[1], all_done, sizeof(int), cudaMemcpyDeviceToHost, st));
+  TD_CUDA(cudaStreamSynchronize(st));
+  *steps_taken = host[0];
+  *done = host[1];
   return TD_OK;
 }
 
@@ -437,12 +623,9 @@ td_status td_adaln_modulate(const void* h, const float* E, const float* phi, int
                             float eps, void* x_mod, void* stream) {
   if (!h || !E || !phi || !x_mod || rows <= 0 || d <= 0 || !(eps >= 0.f))
     return TD_ERR_INVALID_ARG;
-  if (d % 8 != 0 || d > 8 * kAdaThreads * kAdaMaxVec) return TD_ERR_UNSUPPORTED;
+  if (d % 8 != 0 || d > kAdaMaxD) return TD_ERR_UNSUPPORTED;
   if (!aligned16(h) || !aligned16(x_mod)) return TD_ERR_INVALID_ARG;
-  adaln_modulate_kernel<<<rows, kAdaThreads, 0, (cudaStream_t)stream>>>(
-      static_cast<const uint16_t*>(h), E, phi, d, eps, static_cast<uint16_t*>(x_mod), nullptr);
-  TD_CUDA(cudaGetLastError());
-  return TD_OK;
+  return launch_adaln(h, E, phi, rows, d, eps, x_mod, nullptr, (cudaStream_t)stream);
 }
 
 td_status td_block_attention(const td_dims* dims, const void* q, const void* k_blk,
@@ -522,6 +705,15 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
     if (!any) return TD_OK;
   }
   int done = 0;
+  if (t_start <= T) {
+    s = decode_graph(dims, layers, ctx_len, emb, pos, w_lm, phi_table, t_start, T, gamma, tokens,
+                     masked, conf, pred, n_committed, all_done, ws, ws_bytes, st, nsm,
+                     steps_taken, &done);
+    if (s == TD_OK) return done ? TD_OK : TD_ERR_NOT_CONVERGED;
+    if (s != TD_ERR_UNSUPPORTED) return s;
+  }
+  // host loop (when the loop cannot be captured): one all-done read-back per step
+  *steps_taken = 0;
   for (int t = t_start; t <= T; ++t) {
     s = run_step(dims, layers, ctx_len, nullptr, emb, pos, w_lm,
                  phi_table + (size_t)(t - 1) * 6 * dims->d, t, T, gamma, tokens, masked, conf,

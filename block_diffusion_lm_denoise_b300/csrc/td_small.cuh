@@ -15,7 +15,8 @@ namespace td {
 // One CTA per row; 8 bf16 per thread per step.
 __global__ void embed_kernel(const int* __restrict__ tokens, const uint16_t* __restrict__ emb,
                              const uint16_t* __restrict__ pos, uint16_t* __restrict__ h, int S,
-                             int d, int V) {
+                             int d, int V, const int* skip) {
+  if (skip != nullptr && *skip != 0) return;
   const int r = blockIdx.x;
   int tok = tokens[r];
   if (tok < 0 || tok > V) {     // not a vocabulary id nor [MASK]: flag it, read [MASK]
@@ -37,92 +38,132 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const uint16_t* __r
   }
 }
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+// One warp per row, eight rows per CTA. The CTA first stages the modulation vectors
+// (1 + scale) and shift (m = E + phi, fp32) in shared memory; each lane then holds 8-element
+// slices c = 8 lane + 256 k of its row in registers (two-pass mean / variance, warp shuffles).
+constexpr int kAdaRows = 8;
+constexpr int kAdaThreads = 32 * kAdaRows;
+constexpr int kAdaMaxD = 8192;
+
+template <int NK>   // NK = d / 256 slices of 8 elements per lane
+__global__ void __launch_bounds__(kAdaThreads)
+    adaln_modulate_kernel(const uint16_t* __restrict__ h, const float* __restrict__ E,
+                          const float* __restrict__ phi, int rows, int d, float eps,
+                          uint16_t* __restrict__ x_mod, float* __restrict__ gate_out,
+                          const int* skip) {
+  if (skip != nullptr && *skip != 0) return;
+  extern __shared__ float ada_sm[];            // [2][d]: 1 + scale, shift
+  float* one_scale = ada_sm;
+  float* shift = ada_sm + d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    one_scale[c] = 1.0f + (E[d + c] + phi[d + c]);
+    shift[c] = E[c] + phi[c];
+  }
+  if (gate_out != nullptr && blockIdx.x == 0)
+    for (int c = threadIdx.x; c < d; c += blockDim.x) gate_out[c] = E[2 * d + c] + phi[2 * d + c];
   __syncthreads();
-  if (l == 0) red[w] = v;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kAdaRows + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + (size_t)r * d);
+  uint4 raw[NK];
+#pragma unroll
+  for (int k = 0; k < NK; ++k) raw[k] = hr[lane + 32 * k];
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    s += (bf16lo_to_f32(raw[k].x) + bf16hi_to_f32(raw[k].x)) +
+         (bf16lo_to_f32(raw[k].y) + bf16hi_to_f32(raw[k].y)) +
+         (bf16lo_to_f32(raw[k].z) + bf16hi_to_f32(raw[k].z)) +
+         (bf16lo_to_f32(raw[k].w) + bf16hi_to_f32(raw[k].w));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mean = s / (float)d;
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16lo_to_f32(w[j]) - mean, b = bf16hi_to_f32(w[j]) - mean;
+      ss += a * a + b * b;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float rstd = 1.0f / sqrtf(ss / (float)d + eps);
+  uint4* out = reinterpret_cast<uint4*>(x_mod + (size_t)r * d);
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    const int c0 = 8 * (lane + 32 * k);
+    const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + 2 * j;
+      const float y0 = (bf16lo_to_f32(w[j]) - mean) * rstd * one_scale[c] + shift[c];
+      const float y1 = (bf16hi_to_f32(w[j]) - mean) * rstd * one_scale[c + 1] + shift[c + 1];
+      o[j] = pack_bf16x2(y0, y1);
+    }
+    out[lane + 32 * k] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Launch helper: d must be a multiple of 256 for the register path; other multiples of 8
+// take the generic one-CTA-per-row path below.
+__global__ void __launch_bounds__(256)
+    adaln_modulate_generic_kernel(const uint16_t* __restrict__ h, const float* __restrict__ E,
+                                  const float* __restrict__ phi, int d, float eps,
+                                  uint16_t* __restrict__ x_mod, float* __restrict__ gate_out,
+                                  const int* skip) {
+  if (skip != nullptr && *skip != 0) return;
+  __shared__ float red[8];
+  const int r = blockIdx.x;
+  const uint16_t* hr = h + (size_t)r * d;
+  float s = 0.f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) s += __uint_as_float((uint32_t)hr[c] << 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
   __syncthreads();
   float t = 0.f;
   for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
-  return t;
-}
-
-// One CTA (256 threads) per row; the row is held in registers (d <= 256 * 8 * kMaxVec).
-constexpr int kAdaThreads = 256;
-constexpr int kAdaMaxVec = 4;   // d <= 8192
-
-__global__ void __launch_bounds__(kAdaThreads)
-    adaln_modulate_kernel(const uint16_t* __restrict__ h, const float* __restrict__ E,
-                          const float* __restrict__ phi, int d, float eps,
-                          uint16_t* __restrict__ x_mod, float* __restrict__ gate_out) {
-  __shared__ float red[kAdaThreads / 32];
-  const int r = blockIdx.x;
-  const uint4* hr = reinterpret_cast<const uint4*>(h + (size_t)r * d);
-  const int nv = d / 8;
-  float x[kAdaMaxVec][8];
-  float s = 0.f;
-#pragma unroll
-  for (int k = 0; k < kAdaMaxVec; ++k) {
-    const int i = threadIdx.x + k * kAdaThreads;
-    if (i < nv) {
-      const uint4 a = hr[i];
-      x[k][0] = bf16lo_to_f32(a.x); x[k][1] = bf16hi_to_f32(a.x);
-      x[k][2] = bf16lo_to_f32(a.y); x[k][3] = bf16hi_to_f32(a.y);
-      x[k][4] = bf16lo_to_f32(a.z); x[k][5] = bf16hi_to_f32(a.z);
-      x[k][6] = bf16lo_to_f32(a.w); x[k][7] = bf16hi_to_f32(a.w);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s += x[k][j];
-    }
-  }
-  const float mean = block_sum(s, red) / (float)d;
+  const float mean = t / (float)d;
+  __syncthreads();
   float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < kAdaMaxVec; ++k) {
-    const int i = threadIdx.x + k * kAdaThreads;
-    if (i < nv) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float t = x[k][j] - mean;
-        ss += t * t;
-      }
-    }
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    const float a = __uint_as_float((uint32_t)hr[c] << 16) - mean;
+    ss += a * a;
   }
-  const float var = block_sum(ss, red) / (float)d;
-  const float rstd = 1.0f / sqrtf(var + eps);
-  uint4* out = reinterpret_cast<uint4*>(x_mod + (size_t)r * d);
 #pragma unroll
-  for (int k = 0; k < kAdaMaxVec; ++k) {
-    const int i = threadIdx.x + k * kAdaThreads;
-    if (i < nv) {
-      float y[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = i * 8 + j;
-        const float shift = E[c] + phi[c];
-        const float scale = E[d + c] + phi[d + c];
-        y[j] = (x[k][j] - mean) * rstd * (1.0f + scale) + shift;
-      }
-      out[i] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                          pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-    }
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  t = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
+  const float rstd = 1.0f / sqrtf(t / (float)d + eps);
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    const float x = __uint_as_float((uint32_t)hr[c] << 16);
+    const float y = (x - mean) * rstd * (1.0f + (E[d + c] + phi[d + c])) + (E[c] + phi[c]);
+    x_mod[(size_t)r * d + c] = (uint16_t)(pack_bf16x2(y, 0.f) & 0xFFFFu);
   }
-  if (gate_out != nullptr && r == 0) {
+  if (gate_out != nullptr && r == 0)
     for (int c = threadIdx.x; c < d; c += blockDim.x) gate_out[c] = E[2 * d + c] + phi[2 * d + c];
-  }
 }
 
-// One CTA per sequence, 32*S2 threads (S2 = S rounded up to a warp multiple / 32 warps max):
-// warp w merges rows w, w + nwarps, ... over the n_tiles vocabulary partials (increasing
-// vocabulary order, so the lowest id wins ties), then warp 0 applies the commit rule.
-constexpr int kCommitThreads = 256;
-
-__global__ void __launch_bounds__(kCommitThreads)
+// One CTA per sequence, one warp per position (up to 32 warps, looping beyond): a warp merges
+// the row's vocabulary-slice partials (max, lowest argmax, exp-sum), lowest slice first so
+// the lowest id wins ties; then warp 0 applies the commit rule to the sequence.
+__global__ void __launch_bounds__(1024)
     merge_commit_kernel(const float* __restrict__ part_max, const int* __restrict__ part_arg,
                         const float* __restrict__ part_sum, int n_tiles, int S, float gamma,
                         int force_all, int* tokens, unsigned char* masked, float* conf_out,
-                        int* pred_out, int* n_committed, int* all_done, int* counters) {
+                        int* pred_out, int* n_committed, int* all_done, int* counters,
+                        const int* skip, int* steps_taken) {
+  // skip: the decode loop already finished; steps_taken (optional) counts the steps that ran
+  if (skip != nullptr && *skip != 0) return;
+  if (steps_taken != nullptr && blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(steps_taken, 1);
   __shared__ float s_conf[64];
   __shared__ int s_pred[64];
   const int b = blockIdx.x;
@@ -133,25 +174,34 @@ __global__ void __launch_bounds__(kCommitThreads)
     const float* pm = part_max + row * n_tiles;
     const int* pa = part_arg + row * n_tiles;
     const float* ps = part_sum + row * n_tiles;
-    // lane-local pass: max with the lowest tile index on ties (tiles visited in order)
-    float m = -INFINITY;
+    // lane-local pass over slices lane, lane+32, ...: max with the lowest slice on ties,
+    // and the exp-sum relative to a running max (rescaled when it grows)
+    float m = -INFINITY, sum = 0.f;
     int mt = 0x7fffffff;
     for (int t = lane; t < n_tiles; t += 32) {
-      const float v = pm[t];
-      if (v > m) { m = v; mt = t; }
+      const float v = __ldg(&pm[t]);
+      const float sv = __ldg(&ps[t]);
+      if (v > m) {
+        sum = (m == -INFINITY) ? 0.f : sum * ex2_approx((m - v) * 1.4426950408889634f);
+        m = v;
+        mt = t;
+      }
+      sum += sv * ex2_approx((v - m) * 1.4426950408889634f);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
       const int t2 = __shfl_xor_sync(0xffffffffu, mt, o);
-      if (m2 > m || (m2 == m && t2 < mt)) { m = m2; mt = t2; }
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      const float mm = fmaxf(m, m2);
+      const float a = (m == -INFINITY) ? 0.f : sum * ex2_approx((m - mm) * 1.4426950408889634f);
+      const float c = (m2 == -INFINITY) ? 0.f : s2 * ex2_approx((m2 - mm) * 1.4426950408889634f);
+      if (m2 > m || (m2 == m && t2 < mt)) mt = t2;
+      m = mm;
+      sum = a + c;
     }
-    float s = 0.f;
-    for (int t = lane; t < n_tiles; t += 32) s += ps[t] * ex2_approx((pm[t] - m) * 1.4426950408889634f);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) {
-      const float c = 1.0f / s;
+      const float c = 1.0f / sum;
       const int pr = pa[mt];
       s_conf[i] = c;
       s_pred[i] = pr;

@@ -165,7 +165,12 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
  * t = t_start .. T with phi_t = phi_table[t-1] (fp32 [T, 6, d]) and stops after the first
  * step that leaves no position masked. tokens/masked hold the block state on entry
  * (all [MASK] for a fresh block; a partially committed state resumes a stopped loop).
- * steps_taken: HOST int, set to the number of steps run. Reads all_done back once per step.
+ * steps_taken: HOST int, set to the number of steps run.
+ * Execution: the steps t_start..T are captured once per distinct argument set into a CUDA
+ * graph (on a stream private to the library) and replayed on `stream`; every kernel of a step
+ * returns at once when the previous step left nothing masked, so the call synchronises with
+ * the host once per block (plus one read of `masked` on entry). If capture is not possible
+ * the steps run from a host loop that reads all_done back after each step.
  * Returns TD_ERR_NOT_CONVERGED only if positions remain masked after step T (cannot
  * happen with force-commit at t == T; kept for callers that stop early). */
 td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
