@@ -134,6 +134,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // ------------------------------------------------------------------------------------------
 struct AttnPlan {
   int G, Gc, NC, R, n_ctx_tiles, T, n_units, n_teams, ncta, max_seg;
+  bool split;   // some unit is shared by two teams: partials + merge pass
   long long total;
   size_t part_o_bytes, part_ml_bytes;
 };
@@ -157,10 +158,13 @@ AttnPlan plan_attention(const td_dims* dm, int nsm) {
   const int max_teams = std::max(1, nsm / a.NC);
   const int per = (a.n_units + max_teams - 1) / max_teams;
   const int even = (a.n_units + per - 1) / per;
-  if (a.n_units % per == 0 && even * 100 >= max_teams * 85)
+  if (a.n_units % per == 0 && even * 100 >= max_teams * 85) {
     a.n_teams = even;
-  else
+    a.split = false;
+  } else {
     a.n_teams = (int)std::min<long long>(max_teams, a.total);
+    a.split = true;
+  }
   a.ncta = a.n_teams * a.NC;
   const long long tiles = (a.total + a.n_teams - 1) / a.n_teams;
   a.max_seg = (int)((tiles + a.T - 1) / a.T) + 1;
@@ -343,7 +347,7 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
                                                                              mvb, p);
   }
   TD_CUDA(cudaGetLastError());
-  if (a.n_teams != a.n_units) {
+  if (a.split) {
     attn_merge_kernel<<<a.n_units * a.NC, 256, 0, st>>>(p);
     TD_CUDA(cudaGetLastError());
   }

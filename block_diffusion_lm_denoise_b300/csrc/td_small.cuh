@@ -52,15 +52,46 @@ __global__ void __launch_bounds__(kAdaThreads)
                           uint16_t* __restrict__ x_mod, float* __restrict__ gate_out,
                           const int* skip) {
   if (skip != nullptr && *skip != 0) return;
+  constexpr int DD = 256 * NK;                 // d (the launcher checks d == 256 NK)
   extern __shared__ float ada_sm[];            // [2][d]: 1 + scale, shift
-  float* one_scale = ada_sm;
-  float* shift = ada_sm + d;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    one_scale[c] = 1.0f + (E[d + c] + phi[d + c]);
-    shift[c] = E[c] + phi[c];
+  float4* one_scale4 = reinterpret_cast<float4*>(ada_sm);
+  float4* shift4 = reinterpret_cast<float4*>(ada_sm + DD);
+  {
+    // fully unrolled float4 loads, all in flight at once
+    const float4* E4 = reinterpret_cast<const float4*>(E);
+    const float4* P4 = reinterpret_cast<const float4*>(phi);
+    constexpr int PER = DD / 4 / kAdaThreads;   // float4 per thread per vector (NK / 8 ... )
+    static_assert(DD % (4 * kAdaThreads) == 0 || NK < 4, "staging split");
+    if constexpr (DD >= 4 * kAdaThreads) {
+      float4 es[PER], ps[PER], eh[PER], ph[PER];
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int i = threadIdx.x + j * kAdaThreads;
+        es[j] = __ldg(&E4[DD / 4 + i]); ps[j] = __ldg(&P4[DD / 4 + i]);
+        eh[j] = __ldg(&E4[i]); ph[j] = __ldg(&P4[i]);
+      }
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int i = threadIdx.x + j * kAdaThreads;
+        one_scale4[i] = make_float4(1.0f + (es[j].x + ps[j].x), 1.0f + (es[j].y + ps[j].y),
+                                    1.0f + (es[j].z + ps[j].z), 1.0f + (es[j].w + ps[j].w));
+        shift4[i] = make_float4(eh[j].x + ph[j].x, eh[j].y + ph[j].y, eh[j].z + ph[j].z,
+                                eh[j].w + ph[j].w);
+      }
+    } else {
+      for (int i = threadIdx.x; i < DD / 4; i += kAdaThreads) {
+        const float4 es = __ldg(&E4[DD / 4 + i]), ps = __ldg(&P4[DD / 4 + i]);
+        const float4 eh = __ldg(&E4[i]), ph = __ldg(&P4[i]);
+        one_scale4[i] = make_float4(1.0f + (es.x + ps.x), 1.0f + (es.y + ps.y),
+                                    1.0f + (es.z + ps.z), 1.0f + (es.w + ps.w));
+        shift4[i] = make_float4(eh.x + ph.x, eh.y + ph.y, eh.z + ph.z, eh.w + ph.w);
+      }
+    }
   }
   if (gate_out != nullptr && blockIdx.x == 0)
-    for (int c = threadIdx.x; c < d; c += blockDim.x) gate_out[c] = E[2 * d + c] + phi[2 * d + c];
+    for (int c = threadIdx.x; c < DD; c += kAdaThreads) gate_out[c] = E[2 * DD + c] + phi[2 * DD + c];
+  const float* one_scale = ada_sm;
+  const float* shift = ada_sm + DD;
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * kAdaRows + (threadIdx.x >> 5);
