@@ -55,6 +55,7 @@ struct AttnParams {
 
 constexpr int kKSlots = 3;         // K ring (a slot is freed when S of its tile is done)
 constexpr int kVSlots = 4;         // V ring (a slot is freed when PV of its tile is done)
+constexpr int kPrefetch = 4;       // L2 prefetch distance of the producers, in tiles
 constexpr int kAttnThreads = 384;   // 8 softmax warps + 2 producers + 2 MMA issuers
 constexpr int kKProducerWarp = 8;
 constexpr int kVProducerWarp = 9;
@@ -255,8 +256,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int u = u_first; u <= u_last && ok; ++u) {
         const SegInfo s = attn_seg(p, lo, hi, u);
         if (attn_seg_work(p, s) == 0) continue;
+        const int row3 = s.b * p.Hkv + s.g;
+        const int ctx_end = s.t1 < s.nvt ? s.t1 : s.nvt;     // live context tiles end here
+        // L2 prefetch kPrefetch tiles ahead of the ring loads, so that a ring load mostly
+        // hits L2 and its slot turns over in less time
+        for (int t = s.t0; t < s.t0 + kPrefetch && t < ctx_end; ++t)
+          for (int kh = 0; kh < D / 64; ++kh) tma_prefetch_l2_3d(mc, kh * 64, t * kKeyTile, row3);
         for (int t = s.t0; t < s.t1; ++t) {
           if (!attn_tile_live(p, s, t)) continue;
+          if (t + kPrefetch < ctx_end)
+            for (int kh = 0; kh < D / 64; ++kh)
+              tma_prefetch_l2_3d(mc, kh * 64, (t + kPrefetch) * kKeyTile, row3);
           const int st = n % nslot;
           if (n >= nslot && !mbar_wait(&empty[st], ((n / nslot) & 1) ^ 1, ERR_WAIT_MMA)) {
             ok = false;
@@ -265,7 +275,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint8_t* dst = ring + st * L::kKBytes;
           if (t < p.n_ctx_tiles) {
             mbar_arrive_expect_tx(&full[st], kKeyTile * 128 * (D / 64));
-            const int row3 = s.b * p.Hkv + s.g;
             for (int kh = 0; kh < D / 64; ++kh)
               tma_load_3d(dst + kh * L::kKVHalf, mc, &full[st], kh * 64, t * kKeyTile, row3);
           } else {
@@ -543,11 +552,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // Log-sum-exp merge of the partials of every (unit, row chunk) that no single team covered.
-// One CTA per (unit, chunk); thread (row, 4 columns).
-__global__ void attn_merge_kernel(const AttnParams p) {
+// Grid: (unit, chunk) x ceil(R / kMergeRows) row groups; thread (row, 4 columns).
+constexpr int kMergeRows = 16;
+
+__global__ void __launch_bounds__(512) attn_merge_kernel(const AttnParams p) {
   if (p.skip != nullptr && *p.skip != 0) return;
-  const int unit = blockIdx.x / p.NC;
-  const int chunk = blockIdx.x % p.NC;
+  const int uc = blockIdx.x;
+  const int unit = uc / p.NC;
+  const int chunk = uc % p.NC;
   const long long first_tile = (long long)unit * p.T;
   const long long last_tile = first_tile + p.T - 1;
   // team owning a tile x: the largest k with lo(k) <= x (lo is monotone in k)
@@ -566,37 +578,38 @@ __global__ void attn_merge_kernel(const AttnParams p) {
   const int g = unit % p.Hkv;
   const int D = p.D;
   const int nq4 = D / 4;
-  for (int idx = threadIdx.x; idx < p.R * nq4; idx += blockDim.x) {
-    const int r = idx / nq4;
-    const int d4 = idx % nq4;
-    float M = -INFINITY;
-    for (int k = k0; k <= k1; ++k) {
-      const int rec = (k * p.NC + chunk) * p.max_seg +
-                      (unit - (int)(attn_lo(k, p.total, p.n_teams) / p.T));
-      M = fmaxf(M, p.part_ml[((size_t)rec * p.R + r) * 2]);
-    }
-    float Lsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = k0; k <= k1; ++k) {
-      const int rec = (k * p.NC + chunk) * p.max_seg +
-                      (unit - (int)(attn_lo(k, p.total, p.n_teams) / p.T));
-      const float mk = p.part_ml[((size_t)rec * p.R + r) * 2];
-      const float lk = p.part_ml[((size_t)rec * p.R + r) * 2 + 1];
-      if (lk == 0.f) continue;
-      const float w = exp2f(mk - M);
-      Lsum += lk * w;
-      const float4 o = reinterpret_cast<const float4*>(p.part_o + ((size_t)rec * p.R + r) * D)[d4];
-      acc.x += o.x * w; acc.y += o.y * w; acc.z += o.z * w; acc.w += o.w * w;
-    }
-    const float inv = 1.f / Lsum;
-    const int s_tok = r / p.Gc;
-    const int head = g * p.G + chunk * p.Gc + (r % p.Gc);
-    uint16_t* dst = p.out + (((size_t)b * p.S + s_tok) * p.Hq + head) * D + d4 * 4;
-    *reinterpret_cast<uint2*>(dst) =
-        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    if (d4 == 0 && p.lse)
-      p.lse[((size_t)b * p.S + s_tok) * p.Hq + head] = (M + log2f(Lsum)) * 0.6931471805599453f;
+  const int r = blockIdx.y * kMergeRows + threadIdx.x / nq4;
+  if (threadIdx.x >= kMergeRows * nq4 || r >= p.R) return;
+  const int d4 = threadIdx.x % nq4;
+  // at most 4 teams share a unit in practice; larger spans loop
+  float M = -INFINITY;
+  for (int k = k0; k <= k1; ++k) {
+    const int rec = (k * p.NC + chunk) * p.max_seg +
+                    (unit - (int)(attn_lo(k, p.total, p.n_teams) / p.T));
+    M = fmaxf(M, __ldg(&p.part_ml[((size_t)rec * p.R + r) * 2]));
   }
+  float Lsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = k0; k <= k1; ++k) {
+    const int rec = (k * p.NC + chunk) * p.max_seg +
+                    (unit - (int)(attn_lo(k, p.total, p.n_teams) / p.T));
+    const float mk = __ldg(&p.part_ml[((size_t)rec * p.R + r) * 2]);
+    const float lk = __ldg(&p.part_ml[((size_t)rec * p.R + r) * 2 + 1]);
+    if (lk == 0.f) continue;
+    const float w = exp2f(mk - M);
+    Lsum += lk * w;
+    const float4 o =
+        __ldg(reinterpret_cast<const float4*>(p.part_o + ((size_t)rec * p.R + r) * D) + d4);
+    acc.x += o.x * w; acc.y += o.y * w; acc.z += o.z * w; acc.w += o.w * w;
+  }
+  const float inv = 1.f / Lsum;
+  const int s_tok = r / p.Gc;
+  const int head = g * p.G + chunk * p.Gc + (r % p.Gc);
+  uint16_t* dst = p.out + (((size_t)b * p.S + s_tok) * p.Hq + head) * D + d4 * 4;
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (d4 == 0 && p.lse)
+    p.lse[((size_t)b * p.S + s_tok) * p.Hq + head] = (M + log2f(Lsum)) * 0.6931471805599453f;
 }
 
 }  // namespace td

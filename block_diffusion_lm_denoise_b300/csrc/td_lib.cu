@@ -140,9 +140,11 @@ struct AttnPlan {
 };
 
 // Teams of NC CTAs (one per 128-row chunk of a (sequence, KV head) unit) share one key range.
-// If the units split evenly over at least 85% of the possible teams, each team takes whole
-// units and no merge pass is needed; otherwise the (unit, tile) space is cut into one equal
-// range per team (split-K) and the partials are merged.
+//  - at least as many units as teams: if the units split evenly over >= 85% of the possible
+//    teams, each team takes whole units (no merge pass); otherwise the (unit, tile) space is
+//    cut into one equal range per team (split-K) and the partials are merged;
+//  - fewer units than teams: every unit is cut into k = teams / units equal key ranges, so
+//    team boundaries fall on unit boundaries and the merge combines exactly k partials.
 AttnPlan plan_attention(const td_dims* dm, int nsm) {
   AttnPlan a{};
   a.G = dm->Hq / dm->Hkv;
@@ -156,14 +158,20 @@ AttnPlan plan_attention(const td_dims* dm, int nsm) {
   a.n_units = dm->B * dm->Hkv;
   a.total = (long long)a.n_units * a.T;
   const int max_teams = std::max(1, nsm / a.NC);
-  const int per = (a.n_units + max_teams - 1) / max_teams;
-  const int even = (a.n_units + per - 1) / per;
-  if (a.n_units % per == 0 && even * 100 >= max_teams * 85) {
-    a.n_teams = even;
-    a.split = false;
+  if (a.n_units >= max_teams) {
+    const int per = (a.n_units + max_teams - 1) / max_teams;
+    const int even = (a.n_units + per - 1) / per;
+    if (a.n_units % per == 0 && even * 100 >= max_teams * 85) {
+      a.n_teams = even;
+      a.split = false;
+    } else {
+      a.n_teams = max_teams;
+      a.split = true;
+    }
   } else {
-    a.n_teams = (int)std::min<long long>(max_teams, a.total);
-    a.split = true;
+    const int k = std::max(1, std::min(max_teams / a.n_units, a.T));
+    a.n_teams = a.n_units * k;
+    a.split = k > 1;
   }
   a.ncta = a.n_teams * a.NC;
   const long long tiles = (a.total + a.n_teams - 1) / a.n_teams;
@@ -348,7 +356,8 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
   }
   TD_CUDA(cudaGetLastError());
   if (a.split) {
-    attn_merge_kernel<<<a.n_units * a.NC, 256, 0, st>>>(p);
+    const dim3 grid(a.n_units * a.NC, (a.R + kMergeRows - 1) / kMergeRows);
+    attn_merge_kernel<<<grid, kMergeRows * (D / 4), 0, st>>>(p);
     TD_CUDA(cudaGetLastError());
   }
   return TD_OK;
