@@ -38,6 +38,7 @@ constexpr int kKeyTile = 128;
 struct AttnParams {
   int B, S, Hq, Hkv, D, Lmax;
   int G, Gc, NC, R;          // heads per KV head, heads per chunk, chunks per unit, rows per chunk
+  int NCT;                   // CTA pairs per team (pair kernel): ceil(NC / 2)
   int n_ctx_tiles, T;        // ceil(Lmax/128), T = n_ctx_tiles + 1
   int n_units;               // B * Hkv
   int n_teams;               // gridDim.x / NC
@@ -287,7 +288,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (!ok) {
         for (int j = (n > nslot ? n - nslot : 0); j < n; ++j)
-          mbar_wait(&full[j % nslot], (j / nslot) & 1, ERR_WAIT_TMA);
+          mbar_wait_drain(&full[j % nslot], (j / nslot) & 1);
       }
     }
     __syncwarp();
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         cursor_next(c, p, lo, hi, u_last);
       }
       // Let every MMA issued so far finish before the TMEM is released.
-      if (n > 0) mbar_wait(s_full, (n - 1) & 1, ERR_WAIT_MMA);
+      if (n > 0) mbar_wait_drain(s_full, (n - 1) & 1);
     }
     __syncwarp();
   } else if (warp == kPvWarp) {
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mma_commit(&v_empty[st]);
         cursor_next(c, p, lo, hi, u_last);
       }
-      if (n > 0) mbar_wait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, ERR_WAIT_MMA);
+      if (n > 0) mbar_wait_drain(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1);
     }
     __syncwarp();
   } else {

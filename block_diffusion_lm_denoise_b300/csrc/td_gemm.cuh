@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(256, 1)
       // On an aborted run, wait (bounded) for the loads still in flight before leaving.
       if (!ok) {
         for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-          mbar_wait(&full[j % STAGES], (j / STAGES) & 1, ERR_WAIT_TMA);
+          mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1);
       }
     }
     __syncwarp();
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(&acc_full[acc]);
       }
       // Let every MMA issued so far finish before the TMEM is released.
-      if (it > 0) mbar_wait(&empty[(it - 1) % STAGES], ((it - 1) / STAGES) & 1, ERR_WAIT_MMA);
+      if (it > 0) mbar_wait_drain(&empty[(it - 1) % STAGES], ((it - 1) / STAGES) & 1);
     }
     __syncwarp();
   } else if (warp >= 4) {

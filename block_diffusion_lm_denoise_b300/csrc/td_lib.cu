@@ -15,6 +15,7 @@
 
 #include "../../include/td.h"
 #include "td_attention.cuh"
+#include "td_attention_pair.cuh"
 #include "td_gemm.cuh"
 #include "td_ptx.cuh"
 #include "td_small.cuh"
@@ -134,12 +135,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // ------------------------------------------------------------------------------------------
 struct AttnPlan {
   int G, Gc, NC, R, n_ctx_tiles, T, n_units, n_teams, ncta, max_seg;
+  bool pair;    // head_dim 128: two chunks per SM pair (attn_pair_kernel)
+  int NCT;      // pair kernel: CTA pairs per team
   bool split;   // some unit is shared by two teams: partials + merge pass
   long long total;
   size_t part_o_bytes, part_ml_bytes;
 };
 
-// Teams of NC CTAs (one per 128-row chunk of a (sequence, KV head) unit) share one key range.
+// A team walks one key range for all row chunks of its units: NC CTAs (one per 128-row
+// chunk) or, for head_dim 128, ceil(NC / 2) CTA pairs (one chunk per SM of a pair).
 //  - at least as many units as teams: if the units split evenly over >= 85% of the possible
 //    teams, each team takes whole units (no merge pass); otherwise the (unit, tile) space is
 //    cut into one equal range per team (split-K) and the partials are merged;
@@ -153,11 +157,14 @@ AttnPlan plan_attention(const td_dims* dm, int nsm) {
     if (a.G % c == 0 && dm->S * c <= 128) { a.Gc = c; break; }
   a.NC = a.G / a.Gc;
   a.R = dm->S * a.Gc;
+  a.pair = dm->D == 128 && a.NC >= 2;
+  a.NCT = (a.NC + 1) / 2;
   a.n_ctx_tiles = (dm->Lmax + kKeyTile - 1) / kKeyTile;
   a.T = a.n_ctx_tiles + 1;
   a.n_units = dm->B * dm->Hkv;
   a.total = (long long)a.n_units * a.T;
-  const int max_teams = std::max(1, nsm / a.NC);
+  const int team_ctas = a.pair ? 2 * a.NCT : a.NC;
+  const int max_teams = std::max(1, nsm / team_ctas);
   if (a.n_units >= max_teams) {
     const int per = (a.n_units + max_teams - 1) / max_teams;
     const int even = (a.n_units + per - 1) / per;
@@ -173,10 +180,10 @@ AttnPlan plan_attention(const td_dims* dm, int nsm) {
     a.n_teams = a.n_units * k;
     a.split = k > 1;
   }
-  a.ncta = a.n_teams * a.NC;
+  a.ncta = a.n_teams * team_ctas;
   const long long tiles = (a.total + a.n_teams - 1) / a.n_teams;
   a.max_seg = (int)((tiles + a.T - 1) / a.T) + 1;
-  const size_t recs = (size_t)a.ncta * a.max_seg;
+  const size_t recs = (size_t)a.n_teams * a.NC * a.max_seg;
   a.part_o_bytes = align_up(recs * a.R * dm->D * sizeof(float));
   a.part_ml_bytes = align_up(recs * a.R * 2 * sizeof(float));
   return a;
@@ -311,12 +318,18 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
     const uint32_t box[4] = {64, (uint32_t)a.Gc, (uint32_t)dm->S, 1};
     if (!make_map(&mq, q, 4, dims, str, box)) return TD_ERR_CUDA;
   }
+  // K/V boxes: the single-SM kernel loads whole 128-key tiles (block keys: S rows); the pair
+  // kernel loads its half: 64 keys of K, 64 head dims of V (block keys: 64 / 128 rows, the
+  // rows beyond S arrive as zeros)
+  const uint32_t kb_rows = a.pair ? 64 : kKeyTile, vb_rows = kKeyTile;
+  const uint32_t blk_k = a.pair ? 64 : (uint32_t)dm->S, blk_v = a.pair ? 128 : (uint32_t)dm->S;
   {
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)dm->Hkv, (uint64_t)dm->S, (uint64_t)dm->B};
     const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)dm->Hkv * D * 2,
                              (uint64_t)dm->S * dm->Hkv * D * 2};
-    const uint32_t box[4] = {64, 1, (uint32_t)dm->S, 1};
-    if (!make_map(&mkb, k_blk, 4, dims, str, box) || !make_map(&mvb, v_blk, 4, dims, str, box))
+    const uint32_t boxk[4] = {64, 1, blk_k, 1};
+    const uint32_t boxv[4] = {64, 1, blk_v, 1};
+    if (!make_map(&mkb, k_blk, 4, dims, str, boxk) || !make_map(&mvb, v_blk, 4, dims, str, boxv))
       return TD_ERR_CUDA;
   }
   {
@@ -325,15 +338,16 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)(empty ? 1 : dm->Lmax),
                               (uint64_t)(empty ? 1 : dm->B * dm->Hkv)};
     const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)(empty ? 1 : dm->Lmax) * D * 2};
-    const uint32_t box[3] = {64, (uint32_t)kKeyTile, 1};
+    const uint32_t boxk[3] = {64, kb_rows, 1};
+    const uint32_t boxv[3] = {64, vb_rows, 1};
     const void* kb = empty ? k_blk : k_ctx;
     const void* vb = empty ? v_blk : v_ctx;
-    if (!make_map(&mkc, kb, 3, dims, str, box) || !make_map(&mvc, vb, 3, dims, str, box))
+    if (!make_map(&mkc, kb, 3, dims, str, boxk) || !make_map(&mvc, vb, 3, dims, str, boxv))
       return TD_ERR_CUDA;
   }
   AttnParams p{};
   p.B = dm->B; p.S = dm->S; p.Hq = dm->Hq; p.Hkv = dm->Hkv; p.D = D; p.Lmax = dm->Lmax;
-  p.G = a.G; p.Gc = a.Gc; p.NC = a.NC; p.R = a.R;
+  p.G = a.G; p.Gc = a.Gc; p.NC = a.NC; p.NCT = a.NCT; p.R = a.R;
   p.n_ctx_tiles = a.n_ctx_tiles; p.T = a.T; p.n_units = a.n_units; p.n_teams = a.n_teams;
   p.total = a.total;
   p.max_seg = a.max_seg;
@@ -345,7 +359,11 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
   p.out = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  if (D == 128) {
+  if (a.pair) {
+    TD_CUDA(set_smem(attn_pair_kernel, PairSmem::kBytes));
+    attn_pair_kernel<<<a.ncta, kAttnThreads, PairSmem::kBytes, st>>>(mq, mkc, mvc, mkb, mvb,
+                                                                      p);
+  } else if (D == 128) {
     TD_CUDA(set_smem(attn_fused_kernel<128>, AttnSmem<128>::kBytes));
     attn_fused_kernel<128><<<a.ncta, kAttnThreads, AttnSmem<128>::kBytes, st>>>(mq, mkc, mvc, mkb,
                                                                                mvb, p);
@@ -474,6 +492,7 @@ void set_all_smem() {
   set_smem(gemm_tn_kernel<256, 4, EPI_LMHEAD>, GemmSmem<256, 4>::kBytes);
   set_smem(attn_fused_kernel<128>, AttnSmem<128>::kBytes);
   set_smem(attn_fused_kernel<64>, AttnSmem<64>::kBytes);
+  set_smem(attn_pair_kernel, PairSmem::kBytes);
   set_smem(adaln_modulate_kernel<1>, 2 * 256 * 1 * 4);
   set_smem(adaln_modulate_kernel<2>, 2 * 256 * 2 * 4);
   set_smem(adaln_modulate_kernel<4>, 2 * 256 * 4 * 4);
