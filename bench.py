@@ -39,6 +39,34 @@ MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0)
 
 
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "block_diffusion_lm_denoise_b300", "csrc")
+
+
+def traffic_per_launch(kernel: str, sources, units: int):
+    """DRAM bytes (read + write) per launch of `kernel` from the ncu summaries committed under
+    profiles/ ("traffic-record:" lines), scaled from the captured case to `units` (traffic
+    grows in proportion to the units processed). None when no record matches the current
+    sources (the kernel changed since its counters were taken)."""
+    import glob
+    import hashlib
+    h = hashlib.sha1()
+    for f in sources:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    sha = h.hexdigest()
+    for path in sorted(glob.glob(os.path.join(PROFILES, "*.md"))):
+        with open(path) as fh:
+            for line in fh:
+                if not line.startswith("traffic-record:"):
+                    continue
+                f = line.split()
+                kv = dict(x.split("=", 1) for x in f[2:] if "=" in x)
+                if f[1] == kernel and kv.get("sha1") == sha:
+                    return round(int(kv["dram_bytes"]) * units / int(kv["units"]))
+    return None
+
+
 def peaks():
     try:
         with open(MEASURED_PEAKS) as f:
@@ -317,14 +345,20 @@ def main():
     step_ms = ms / max(1, total_steps)
     attn_share = dm.n_layers * attn_ms / step_ms
     lm_share = lm_ms / step_ms
-    roof_attn = {"kernel": "attn_fused_kernel<128> (+merge)", "bound": "hbm",
+    attn_kernel = "attn_pair_kernel"   # head_dim 128 with two or more 128-row chunks per unit
+    attn_traffic = traffic_per_launch(
+        attn_kernel, ["td_ptx.cuh", "td_attention.cuh", "td_attention_pair.cuh"],
+        dm.B * dm.Hkv * dm.Lmax)
+    lm_kernel = "gemm_tn_kernel<256,4,EPI_LMHEAD>"
+    lm_traffic = traffic_per_launch(lm_kernel, ["td_ptx.cuh", "td_gemm.cuh"], M)
+    roof_attn = {"kernel": attn_kernel, "bound": "hbm",
                  "achieved": round(attn_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                 "frac": round(attn_gbs / pk["hbm_gbs"], 4), "traffic": None,
+                 "frac": round(attn_gbs / pk["hbm_gbs"], 4), "traffic": attn_traffic,
                  "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(attn_ms, 4),
                  "share_of_step": round(attn_share, 3), "peak_source": pk_kind}
-    roof_lm = {"kernel": "gemm_tn_kernel<256,4,LMHEAD> + merge_commit", "bound": "tensor",
+    roof_lm = {"kernel": lm_kernel + " + merge_commit", "bound": "tensor",
                "achieved": round(lm_tflops, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-               "frac": round(lm_tflops / pk["bf16_tflops"], 4), "traffic": None,
+               "frac": round(lm_tflops / pk["bf16_tflops"], 4), "traffic": lm_traffic,
                "algorithmic_flops_per_launch": lm_flops, "ms_per_launch": round(lm_ms, 4),
                "share_of_step": round(lm_share, 3), "peak_source": pk_kind}
     dominant, other = (roof_attn, roof_lm) if attn_share >= lm_share else (roof_lm, roof_attn)
