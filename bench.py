@@ -363,7 +363,8 @@ def main():
                "share_of_step": round(lm_share, 3), "peak_source": pk_kind}
     dominant, other = (roof_attn, roof_lm) if attn_share >= lm_share else (roof_lm, roof_attn)
 
-    launches_per_step = 1 + dm.n_layers * 4 + 2   # embed, 6 x (adaLN, QKV, attention, O-proj), LM, commit
+    # embed, LM row map, 6 x (adaLN, QKV, attention, O-proj), LM head, commit
+    launches_per_step = 2 + dm.n_layers * 4 + 2
     result = {
         "metric": "committed tokens/sec (block decode, S=16, gamma=0.8)",
         "value": round(value, 1),

@@ -1,7 +1,8 @@
 // td_gemm.cuh -- persistent tcgen05 GEMM  C[M, N] = A[M, K] * B[N, K]^T  (bf16 in, fp32
 // accumulate in TMEM) with three fused epilogues:
 //   EPI_QKV    : bf16 store of the [q | k | v] projection into three row-major tensors
-//   EPI_RESID  : gated residual  h[r, n] = bf16(h[r, n] + gate[n] * C[r, n])  (in place)
+//   EPI_RESID  : gated residual  h[r, n] = bf16(h[r, n] + gate[n] * C[r, n])  (in place, or
+//                for the last layer of a step only the rows the LM head needs, compacted)
 //   EPI_LMHEAD : per row and per 128/256-column vocabulary tile, (max, lowest argmax,
 //                sum of exp(z - max)) of the logits; the logits are never written.
 //
@@ -28,15 +29,21 @@ struct GemmParams {
   uint16_t* k;
   uint16_t* v;
   int nq, nk;
-  // EPI_RESID
+  // EPI_RESID; with row_pos set, row r's result goes to row row_pos[r] of h_out instead of
+  // back into h, and rows with row_pos[r] < 0 are not written
   uint16_t* h;
   const float* gate;
+  const int* row_pos;
+  uint16_t* h_out;
   // EPI_LMHEAD partials, [M][n_tiles] each
   float* part_max;
   int* part_arg;
   float* part_sum;
   // when non-null and nonzero, the kernel returns at once (a finished decode loop)
   const int* skip;
+  // when non-null: only the first *m_count rows of A are live (read on the device; M is the
+  // row capacity of A and of the partials)
+  const int* m_count;
 };
 
 template <int BN, int STAGES>
@@ -66,6 +73,10 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nkb = p.K / 64;
+  const int M = p.m_count != nullptr ? min(max(*p.m_count, 0), p.M) : p.M;
+  const int m_tiles = (M + 127) / 128;
+  const int items = m_tiles * p.n_tiles;
+  if (blockIdx.x >= items) return;   // before any barrier or TMEM allocation
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -94,9 +105,9 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
-        const int mt = item % p.m_tiles;
-        const int nt = item / p.m_tiles;
+      for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+        const int mt = item % m_tiles;
+        const int nt = item / m_tiles;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -123,7 +134,7 @@ __global__ void __launch_bounds__(256, 1)
       constexpr uint32_t idesc = idesc_bf16(128, BN, 0);
       int it = 0, lt = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++lt) {
+      for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++lt) {
         const int acc = lt & 1;
         const int use = lt >> 1;
         if (lt >= 2 && !mbar_wait(&acc_empty[acc], (use & 1) ^ 1, ERR_WAIT_EPI)) {
@@ -160,15 +171,19 @@ __global__ void __launch_bounds__(256, 1)
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
     int lt = 0;
-    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++lt) {
-      const int mt = item % p.m_tiles;
-      const int nt = item / p.m_tiles;
+    for (int item = blockIdx.x; item < items; item += gridDim.x, ++lt) {
+      const int mt = item % m_tiles;
+      const int nt = item / m_tiles;
       const int acc = lt & 1;
       if (!mbar_wait(&acc_full[acc], (lt >> 1) & 1, ERR_WAIT_MMA)) break;
       tc_fence_after();
       const int row = mt * 128 + row_in_tile;
-      const bool row_ok = row < p.M;
+      const bool row_ok = row < M;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      int out_row = row;
+      if constexpr (EPI == EPI_RESID) {
+        if (p.row_pos != nullptr) out_row = row_ok ? p.row_pos[row] : -1;
+      }
 
       float run_max = -INFINITY, run_sum = 0.f;
       int run_arg = 0;
@@ -220,8 +235,10 @@ __global__ void __launch_bounds__(256, 1)
             }
           }
         } else {  // EPI_RESID
-          if (row_ok && col0 < p.N) {
-            uint4* h4 = reinterpret_cast<uint4*>(p.h + (size_t)row * p.N + col0);
+          if (row_ok && col0 < p.N && out_row >= 0) {
+            const uint4* h4 = reinterpret_cast<const uint4*>(p.h + (size_t)row * p.N + col0);
+            uint4* o4 = reinterpret_cast<uint4*>(
+                (p.row_pos != nullptr ? p.h_out : p.h) + (size_t)out_row * p.N + col0);
             const float4* g4 = reinterpret_cast<const float4*>(p.gate + col0);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -237,7 +254,7 @@ __global__ void __launch_bounds__(256, 1)
                                 bf16hi_to_f32(hv.z) + gb.y * v[8 * j + 5]);
               w.w = pack_bf16x2(bf16lo_to_f32(hv.w) + gb.z * v[8 * j + 6],
                                 bf16hi_to_f32(hv.w) + gb.w * v[8 * j + 7]);
-              h4[j] = w;
+              o4[j] = w;
             }
           }
         }

@@ -273,11 +273,14 @@ td_status launch_adaln(const void* h, const float* E, const float* phi, int rows
   return TD_OK;
 }
 
+// With row_pos / m_count set, h holds only the rows masked at the step start (compacted,
+// *m_count of them on the device) and the other rows are reported as not evaluated.
 td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, float gamma,
                             int force_all, int* tokens, unsigned char* masked, float* conf,
                             int* pred, int* n_committed, int* all_done, void* ws,
                             cudaStream_t st, int nsm, const int* skip = nullptr,
-                            int* steps = nullptr) {
+                            int* steps = nullptr, const int* row_pos = nullptr,
+                            const int* m_count = nullptr) {
   const int M = dm->B * dm->S;
   const int V = dm->V;
   const int bn = lm_bn(M);
@@ -293,13 +296,14 @@ td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, 
   gp.part_arg = parg;
   gp.part_sum = psum;
   gp.skip = skip;
+  gp.m_count = m_count;
   td_status s = gemm_dispatch<EPI_LMHEAD>(h, w_lm, M, V, dm->d, gp, st, nsm, bn);
   if (s != TD_OK) return s;
   TD_CUDA(cudaMemsetAsync(counters, 0, 2 * sizeof(int), st));
   merge_commit_kernel<<<dm->B, 32 * std::min(dm->S, 32), 0, st>>>(pmax, parg, psum, nt, dm->S, gamma,
                                                          force_all, tokens, masked, conf, pred,
                                                          n_committed, all_done, counters,
-                                                         skip, steps);
+                                                         skip, steps, row_pos);
   TD_CUDA(cudaGetLastError());
   return TD_OK;
 }
@@ -386,6 +390,9 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
 // ------------------------------------------------------------------------------------------
 struct StepWs {
   uint16_t *h, *xmod, *q, *k, *v, *o;
+  uint16_t* h_lm;   // last layer's output, rows masked at the step start only (compacted)
+  int* row_pos;     // [B*S] compact index of each row, -1 if committed
+  int* m_count;     // number of rows in h_lm
   float* gate;
   void* attn;
   void* lm;
@@ -405,6 +412,7 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
   const size_t o_h = take(M * dm->d * 2), o_x = take(M * dm->d * 2);
   const size_t o_q = take(M * dm->Hq * dm->D * 2), o_k = take(M * dm->Hkv * dm->D * 2),
                o_v = take(M * dm->Hkv * dm->D * 2), o_o = take(M * dm->Hq * dm->D * 2);
+  const size_t o_hl = take(M * dm->d * 2), o_rp = take(M * 4), o_mc = take(16);
   const size_t o_g = take((size_t)dm->d * 4);
   const size_t o_a = take(attn_ws_bytes(dm, nsm));
   const size_t o_l = take(lm_ws_bytes((int)M, dm->V));
@@ -418,6 +426,9 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
     w.k = reinterpret_cast<uint16_t*>(b + o_k);
     w.v = reinterpret_cast<uint16_t*>(b + o_v);
     w.o = reinterpret_cast<uint16_t*>(b + o_o);
+    w.h_lm = reinterpret_cast<uint16_t*>(b + o_hl);
+    w.row_pos = reinterpret_cast<int*>(b + o_rp);
+    w.m_count = reinterpret_cast<int*>(b + o_mc);
     w.gate = reinterpret_cast<float*>(b + o_g);
     w.attn = b + o_a;
     w.lm = b + o_l;
@@ -442,6 +453,10 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
     TD_CUDA(cudaMemcpyAsync(w.h, h, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st));
   }
   TD_CUDA(cudaGetLastError());
+  // the LM head evaluates only the rows still masked now: the last layer writes them,
+  // compacted, into h_lm
+  lm_rows_kernel<<<1, kRowsThreads, 0, st>>>(masked, M, w.row_pos, w.m_count, skip);
+  TD_CUDA(cudaGetLastError());
   const int nq = dm->Hq * dm->D, nk = dm->Hkv * dm->D;
   const int bn = M >= 512 ? 256 : 128;
   for (int l = 0; l < dm->n_layers; ++l) {
@@ -457,11 +472,20 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
     if (s != TD_OK) return s;
     GemmParams g2{};
     g2.h = w.h; g2.gate = w.gate; g2.skip = skip;
+    if (l == dm->n_layers - 1) {
+      g2.row_pos = w.row_pos;
+      g2.h_out = w.h_lm;
+    }
     s = gemm_dispatch<EPI_RESID>(w.o, L.wo, M, d, nq, g2, st, nsm, bn);
     if (s != TD_OK) return s;
   }
-  return run_lmhead_commit(dm, w.h, w_lm, gamma, t == T ? 1 : 0, tokens, masked, conf, pred,
-                           n_committed, all_done, w.lm, st, nsm, skip, steps);
+  if (dm->n_layers == 0) {
+    gather_rows_kernel<<<M, 256, 0, st>>>(w.h, w.row_pos, w.h_lm, d, skip);
+    TD_CUDA(cudaGetLastError());
+  }
+  return run_lmhead_commit(dm, w.h_lm, w_lm, gamma, t == T ? 1 : 0, tokens, masked, conf, pred,
+                           n_committed, all_done, w.lm, st, nsm, skip, steps, w.row_pos,
+                           w.m_count);
 }
 
 td_status check_layers(const td_dims* dm, const td_layer* layers) {

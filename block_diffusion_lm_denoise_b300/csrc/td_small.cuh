@@ -183,6 +183,59 @@ __global__ void __launch_bounds__(256)
     for (int c = threadIdx.x; c < d; c += blockDim.x) gate_out[c] = E[2 * d + c] + phi[2 * d + c];
 }
 
+// Rows the LM head evaluates in a denoise step: those still masked when the step starts
+// (committed rows need no logits). One CTA of kRowsThreads threads; thread t owns the
+// contiguous rows [t * per, (t + 1) * per). row_pos[r] = index of row r among the masked rows
+// (row order kept), or -1; *count = number of masked rows.
+constexpr int kRowsThreads = 1024;
+
+__global__ void __launch_bounds__(kRowsThreads)
+    lm_rows_kernel(const unsigned char* __restrict__ masked, int M, int* __restrict__ row_pos,
+                   int* __restrict__ count, const int* skip) {
+  if (skip != nullptr && *skip != 0) return;
+  __shared__ int warp_tot[kRowsThreads / 32];
+  const int per = (M + kRowsThreads - 1) / kRowsThreads;
+  const int r0 = min(M, (int)threadIdx.x * per), r1 = min(M, r0 + per);
+  int n = 0;
+  for (int r = r0; r < r1; ++r) n += masked[r] != 0;
+  // exclusive scan of n over the block: within the warp, then over the warp totals
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_tot[lane] = w;   // inclusive over warps
+  }
+  __syncthreads();
+  int base = incl - n + (warp > 0 ? warp_tot[warp - 1] : 0);
+  for (int r = r0; r < r1; ++r) row_pos[r] = masked[r] != 0 ? base++ : -1;
+  if (threadIdx.x == kRowsThreads - 1) *count = warp_tot[31];
+}
+
+// Copies row r of h to row row_pos[r] of h_out when row_pos[r] >= 0 (a step without layers:
+// the caller's hidden states go to the LM head as they are). One CTA per row.
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ h, const int* __restrict__ row_pos,
+                                   uint16_t* __restrict__ h_out, int d, const int* skip) {
+  if (skip != nullptr && *skip != 0) return;
+  const int r = blockIdx.x;
+  const int rp = row_pos[r];
+  if (rp < 0) return;
+  const uint4* src = reinterpret_cast<const uint4*>(h + (size_t)r * d);
+  uint4* dst = reinterpret_cast<uint4*>(h_out + (size_t)rp * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+}
+
 // One CTA per sequence, one warp per position (up to 32 warps, looping beyond): a warp merges
 // the row's vocabulary-slice partials (max, lowest argmax, exp-sum), lowest slice first so
 // the lowest id wins ties; then warp 0 applies the commit rule to the sequence.
@@ -191,8 +244,10 @@ __global__ void __launch_bounds__(1024)
                         const float* __restrict__ part_sum, int n_tiles, int S, float gamma,
                         int force_all, int* tokens, unsigned char* masked, float* conf_out,
                         int* pred_out, int* n_committed, int* all_done, int* counters,
-                        const int* skip, int* steps_taken) {
-  // skip: the decode loop already finished; steps_taken (optional) counts the steps that ran
+                        const int* skip, int* steps_taken, const int* row_pos) {
+  // skip: the decode loop already finished; steps_taken (optional) counts the steps that ran;
+  // row_pos (optional): the partials hold only the rows masked at the step start, row r at
+  // row_pos[r]; the other rows were not evaluated and get conf 0, pred -1
   if (skip != nullptr && *skip != 0) return;
   if (steps_taken != nullptr && blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(steps_taken, 1);
   __shared__ float s_conf[64];
@@ -202,9 +257,23 @@ __global__ void __launch_bounds__(1024)
   const int nwarps = blockDim.x >> 5;
   for (int i = warp; i < S; i += nwarps) {
     const size_t row = (size_t)b * S + i;
-    const float* pm = part_max + row * n_tiles;
-    const int* pa = part_arg + row * n_tiles;
-    const float* ps = part_sum + row * n_tiles;
+    size_t prow = row;
+    if (row_pos != nullptr) {
+      const int rp = row_pos[row];
+      if (rp < 0) {
+        if (lane == 0) {
+          s_conf[i] = 0.f;
+          s_pred[i] = -1;
+          conf_out[row] = 0.f;
+          pred_out[row] = -1;
+        }
+        continue;
+      }
+      prow = (size_t)rp;
+    }
+    const float* pm = part_max + prow * n_tiles;
+    const int* pa = part_arg + prow * n_tiles;
+    const float* ps = part_sum + prow * n_tiles;
     // lane-local pass over slices lane, lane+32, ...: max with the lowest slice on ties,
     // and the exp-sum relative to a running max (rescaled when it grows)
     float m = -INFINITY, sum = 0.f;

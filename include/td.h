@@ -150,7 +150,10 @@ td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm,
  *   m = E_l + phi_t; x_mod = adaLN(h) as in td_adaln_modulate (eps = 1e-6);
  *   [q | k | v] = bf16(x_mod . wqkv^T); o = td_block_attention(...);
  *   h = bf16(h + m[2] * (o . wo^T))            (m[2] is the gate)
- * and finally td_lmhead_commit with force_all = (t == T).
+ * and finally td_lmhead_commit with force_all = (t == T), evaluated only on the rows that
+ * are masked when the step starts (committed rows need no logits; the last layer writes just
+ * those rows, compacted, and the LM head reads their count on the device). Rows already
+ * committed when the step starts get conf = 0 and pred = -1.
  *   phi_t fp32 [6, d]: the shared adaLN-single timestep vector of step t (1 <= t <= T).
  *   layers: HOST array of dims->n_layers td_layer structs (device pointers inside).
  *   ctx_len int32 [B] device or NULL.  Other outputs as in td_lmhead_commit. */

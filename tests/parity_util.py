@@ -54,17 +54,24 @@ def excluded_sequences(conf_ref, gap_ref, masked_before, gamma: float):
     return ex
 
 
-def compare_commit(ref: dict, gpu: dict, masked_before, gamma: float):
+def compare_commit(ref: dict, gpu: dict, masked_before, gamma: float, step: bool = False):
     """ref: oracle outputs (conf, pred, gap, tokens, masked); gpu: numpy arrays of the same.
+    step=True: the GPU side is a denoise step, which evaluates the LM head only on the rows
+    masked when the step starts and reports conf 0, pred -1 on the others.
     Returns a report dict; raises AssertionError on a mismatch outside the exclusions."""
     conf_ref = np.asarray(ref["conf"], np.float64)
     gap = np.asarray(ref["gap"], np.float64)
     conf_gpu = np.asarray(gpu["conf"], np.float64)
-    dconf = np.abs(conf_gpu - conf_ref)
-    assert dconf.max() <= CONF_TOL, f"conf error {dconf.max()}"
+    pred_gpu = np.asarray(gpu["pred"])
+    evaluated = np.asarray(masked_before, bool) if step else np.ones(conf_ref.shape, bool)
+    if step:
+        assert (conf_gpu[~evaluated] == 0).all() and (pred_gpu[~evaluated] == -1).all(), \
+            "rows committed before the step must read conf 0, pred -1"
+    dconf = np.where(evaluated, np.abs(conf_gpu - conf_ref), 0.0)
+    assert dconf.max(initial=0.0) <= CONF_TOL, f"conf error {dconf.max()}"
     ex_seq = excluded_sequences(conf_ref, gap, masked_before, gamma)
     tie_pos = gap < GAP_BAND
-    pred_bad = (np.asarray(gpu["pred"]) != np.asarray(ref["pred"])) & ~tie_pos
+    pred_bad = (pred_gpu != np.asarray(ref["pred"])) & ~tie_pos & evaluated
     assert not pred_bad.any(), f"pred mismatch at {np.argwhere(pred_bad)[:8]}"
     mk_bad = (np.asarray(gpu["masked"], bool) != np.asarray(ref["masked"], bool))
     mk_bad[ex_seq] = False

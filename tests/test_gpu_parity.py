@@ -228,7 +228,7 @@ def test_denoise_step_tiny_matches_oracle(cuda_device):
                             wl.T, h=wl.h)
     compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
                            tokens=wl.tokens.cpu().numpy(), masked=wl.masked.cpu().numpy()),
-                   m0.cpu().numpy(), wl.gamma)
+                   m0.cpu().numpy(), wl.gamma, step=True)
 
 
 def test_denoise_step_embed_path_and_stacked_layers(cuda_device):
@@ -260,7 +260,44 @@ def test_denoise_step_embed_path_and_stacked_layers(cuda_device):
                             ctx_len=[200, 64, 13])
     compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
                            tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
-                   m0.cpu().numpy(), 0.8)
+                   m0.cpu().numpy(), 0.8, step=True)
+
+
+@pytest.mark.parametrize("n_layers", [0, 2])
+def test_denoise_step_evaluates_only_rows_masked_at_step_start(cuda_device, n_layers):
+    # sequence 0 fully masked, sequence 1 fully committed, sequence 2 one masked position in
+    # the middle: the LM head runs on 16 + 1 compacted rows
+    seed = 23
+    dm = synth.Dims(B=3, S=16, d=256, Hq=8, Hkv=2, D=64, V=1024, Lmax=150, n_layers=n_layers)
+    layers = [synth._layer(seed, l, dm, 1 / 16, 1 / math.sqrt(dm.Hq * dm.D), 1.0, cuda_device)
+              for l in range(dm.n_layers)]
+    w_lm = synth.normal((dm.V, dm.d), 0.05, seed, "w_lm", cuda_device)
+    h = synth.normal((dm.B * dm.S, dm.d), 1.0, seed, "h", cuda_device)
+    phi = synth.phi_table(16, dm.d, seed, cuda_device)
+    masked = torch.zeros((dm.B, dm.S), dtype=torch.uint8, device=cuda_device)
+    masked[0] = 1
+    masked[2, 7] = 1
+    tokens = torch.where(masked.bool(), torch.full((dm.B, dm.S), dm.V, dtype=torch.int32,
+                                                   device=cuda_device),
+                         synth.integers((dm.B, dm.S), dm.V, seed, "tok", cuda_device))
+    t0, m0 = tokens.clone(), masked.clone()
+    conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[2], 3, 16, 0.8,
+                                                tokens, masked, h=h)
+    torch.cuda.synchronize()
+    _no_device_error()
+    r = oracle.denoise_step(dm.as_dict(), layers, phi[2], w_lm, t0.cpu().numpy(),
+                            m0.cpu().numpy().astype(bool), 0.8, 3, 16, h=h)
+    compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                           tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
+                   m0.cpu().numpy(), 0.8, step=True)
+    assert ncom[1].item() == 0 and ncom[2].item() == 1 and ncom[0].item() >= 1
+    assert torch.equal(tokens[1], t0[1])
+    # nothing masked at all: no row is evaluated, nothing commits, the block is done
+    conf2, pred2, ncom2, done2 = td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[2], 3, 16,
+                                                    0.8, tokens, torch.zeros_like(masked), h=h)
+    torch.cuda.synchronize()
+    assert torch.all(conf2 == 0) and torch.all(pred2 == -1) and torch.all(ncom2 == 0)
+    assert int(done2.item()) == 1
 
 
 def test_denoise_step_mid_size(cuda_device):
@@ -277,7 +314,7 @@ def test_denoise_step_mid_size(cuda_device):
                             wl.T, h=wl.h)
     rep = compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
                                  tokens=wl.tokens.cpu().numpy(), masked=wl.masked.cpu().numpy()),
-                         m0.cpu().numpy(), wl.gamma)
+                         m0.cpu().numpy(), wl.gamma, step=True)
     frac = float((r["conf"][m0.cpu().numpy().astype(bool)] >= 0.8).mean())
     print("mid step:", rep, "fraction of masked rows with conf >= 0.8:", frac)
 
@@ -335,7 +372,7 @@ def test_decode_loop_full_size_sampled(cuda_device):
                                 t, wl.T, emb=emb_cpu, pos=pos_cpu)
         rep = compare_commit(r, dict(conf=rec["conf"][seqs], pred=rec["pred"][seqs],
                                      tokens=rec["tokens"][seqs], masked=rec["masked"][seqs]),
-                             msk, wl.gamma)
+                             msk, wl.gamma, step=True)
         if rep["excluded_sequences"]:
             print("decode loop: stopped comparing at step", t, rep)
             break
