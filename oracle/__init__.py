@@ -6,6 +6,8 @@ import this package. See ``td_oracle`` for the method, its sources and its readi
 
 from .td_oracle import (  # noqa: F401
     LN_EPS,
+    RULE_CONFIDENCE,
+    RULE_LEFT_TO_RIGHT,
     adaln_modulate,
     adaln_vectors,
     as_f64,
@@ -15,6 +17,7 @@ from .td_oracle import (  # noqa: F401
     decode_block,
     denoise_step,
     embed,
+    kv_append,
     layer_forward,
     layer_norm,
     lmhead_confidence,

@@ -213,11 +213,20 @@ def lmhead_confidence(h, w_lm, rows: Optional[Sequence[int]] = None, chunk: int 
 # Commit rule ([chathome] generation + evaluation paragraphs; reading R6)
 # ----------------------------------------------------------------------------------------
 
-def commit(conf, pred, tokens, masked, gamma: float, force_all: bool):
-    """Apply the confidence-masking commit rule to each sequence.
+RULE_CONFIDENCE = 0       # mask-diffusion mode: confidence masking with threshold gamma
+RULE_LEFT_TO_RIGHT = 1    # mock-AR reading: exactly one position per step, left to right
+
+
+def commit(conf, pred, tokens, masked, gamma: float, force_all: bool,
+           rule: int = RULE_CONFIDENCE):
+    """Apply the commit rule to each sequence.
 
     conf [B, S] (fp64), pred [B, S], tokens [B, S] int, masked [B, S] bool.
     gamma is the float32 threshold widened to fp64, so both sides compare with one number.
+    rule RULE_CONFIDENCE: {masked i : conf_i >= gamma}, else the most confident masked
+    position (lowest index on ties). rule RULE_LEFT_TO_RIGHT (the pages name a mock-AR mode
+    without defining it; read as the AR order inside the block): the lowest-index masked
+    position, whatever its confidence. force_all (step T) commits every masked position.
     Returns (tokens', masked', n_committed [B], committed [B, S] bool).
     """
     conf = np.asarray(conf, dtype=np.float64)
@@ -229,6 +238,8 @@ def commit(conf, pred, tokens, masked, gamma: float, force_all: bool):
     for b in range(B):
         if force_all:
             chosen = [i for i in range(S) if masked[b, i]]
+        elif rule == RULE_LEFT_TO_RIGHT:
+            chosen = [i for i in range(S) if masked[b, i]][:1]
         else:
             chosen = [i for i in range(S) if masked[b, i] and conf[b, i] >= g]
             if not chosen and masked[b].any():
@@ -276,7 +287,7 @@ def layer_forward(h, layer, phi, dims, ctx_len=None):
 
 
 def denoise_step(dims, layers, phi_t, w_lm, tokens, masked, gamma, t, T,
-                 h=None, emb=None, pos=None, ctx_len=None):
+                 h=None, emb=None, pos=None, ctx_len=None, rule: int = RULE_CONFIDENCE):
     """One denoising step: embed (if h is None), every layer, LM head, commit.
 
     Returns a dict with conf, pred, gap, tokens, masked, n_committed, committed, h_final.
@@ -290,13 +301,15 @@ def denoise_step(dims, layers, phi_t, w_lm, tokens, masked, gamma, t, T,
         h, _ = layer_forward(h, layer, phi_t, dims, ctx_len)
     conf, pred, gap, zmax = lmhead_confidence(h, w_lm)
     conf = conf.reshape(B, S); pred = pred.reshape(B, S); gap = gap.reshape(B, S)
-    tok2, msk2, ncom, committed = commit(conf, pred, tokens, masked, gamma, force_all=(t == T))
+    tok2, msk2, ncom, committed = commit(conf, pred, tokens, masked, gamma, force_all=(t == T),
+                                         rule=rule)
     return dict(conf=conf, pred=pred, gap=gap, zmax=zmax.reshape(B, S), tokens=tok2,
                 masked=msk2, n_committed=ncom, committed=committed, h_final=h)
 
 
 def decode_block(dims, layers, phi_table, w_lm, emb, pos, gamma, T, tokens=None, masked=None,
-                 t_start: int = 1, ctx_len=None, trace: bool = False):
+                 t_start: int = 1, ctx_len=None, trace: bool = False,
+                 rule: int = RULE_CONFIDENCE):
     """Block decode loop: starting from all [MASK] (or a given state), run steps
     t = t_start..T, stop after the first step that leaves nothing masked.
 
@@ -314,7 +327,7 @@ def decode_block(dims, layers, phi_table, w_lm, emb, pos, gamma, T, tokens=None,
         if not masked.any():
             break
         r = denoise_step(dims, layers, phi_table[t - 1], w_lm, tokens, masked, gamma, t, T,
-                         emb=emb, pos=pos, ctx_len=ctx_len)
+                         emb=emb, pos=pos, ctx_len=ctx_len, rule=rule)
         tokens, masked = r["tokens"], r["masked"]
         steps += 1
         if trace:
@@ -322,3 +335,37 @@ def decode_block(dims, layers, phi_table, w_lm, emb, pos, gamma, T, tokens=None,
         if not masked.any():
             break
     return tokens, masked, steps, records
+
+
+# ----------------------------------------------------------------------------------------
+# Context cache growth ([chathome] generation paragraph: once a block is committed, the
+# context tower takes it in and the next block attends to it)
+# ----------------------------------------------------------------------------------------
+
+def kv_append(k_ctx, v_ctx, ctx_len, k_new, v_new):
+    """Append one committed block's keys / values to a layer's context cache.
+
+    k_ctx, v_ctx [B, Hkv, Lmax, D]; ctx_len [B]; k_new, v_new [B, S, Hkv, D] (the context
+    tower's keys / values of the block, token-major as a projection yields them).
+    Row ctx_len[b] + i of head g receives token i of head g. Sequences whose cache would
+    overflow (ctx_len[b] + S > Lmax) are left unchanged and reported.
+    Returns (k_ctx', v_ctx', ctx_len', overflow [B] bool); inputs are not modified.
+    """
+    k = np.array(as_f64(k_ctx), copy=True)
+    v = np.array(as_f64(v_ctx), copy=True)
+    kn = as_f64(k_new)
+    vn = as_f64(v_new)
+    B, Hkv, Lmax, D = k.shape
+    S = kn.shape[1]
+    ln = np.array(ctx_len, dtype=np.int64, copy=True)
+    overflow = np.zeros(B, dtype=bool)
+    for b in range(B):
+        L = int(ln[b])
+        if L < 0 or L + S > Lmax:
+            overflow[b] = True
+            continue
+        for g in range(Hkv):
+            k[b, g, L:L + S, :] = kn[b, :, g, :]
+            v[b, g, L:L + S, :] = vn[b, :, g, :]
+        ln[b] = L + S
+    return k, v, ln, overflow

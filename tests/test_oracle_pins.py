@@ -418,3 +418,73 @@ def test_brute_force_step_on_tiny_inputs():
         cf = 1.0 / sum(math.exp(zz - zm) for zz in z[rr])
         assert abs(cf - r["conf"][0, rr]) < 1e-6
         assert z[rr].index(zm) == r["pred"][0, rr]
+
+
+# ----------------------------------------------------------------------------- mock-AR reading
+
+def test_commit_left_to_right_golden_cases():
+    with open(os.path.join(GOLDEN, "commit_left_to_right.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        conf = np.float32(c["conf"]).astype(np.float64)[None]
+        tok, msk, n, com = oracle.commit(conf, np.array(c["pred"])[None], np.array(c["tokens"])[None],
+                                         np.array(c["masked"], bool)[None], c["gamma"], c["force_all"],
+                                         rule=oracle.RULE_LEFT_TO_RIGHT)
+        assert list(np.nonzero(com[0])[0]) == c["expect_committed"], c["name"]
+        assert list(tok[0]) == c["expect_tokens"], c["name"]
+        assert n[0] == len(c["expect_committed"])
+
+
+def test_left_to_right_decode_commits_positions_in_order_one_per_step():
+    dm = synth.Dims(B=2, S=6, d=64, Hq=2, Hkv=1, D=64, V=50, Lmax=5, n_layers=1)
+    L = synth._layer(3, 0, dm, 1 / 8, 1 / 8, 1.0, "cpu")
+    emb = synth.normal((dm.V + 1, dm.d), 1.0, 3, "emb")
+    pos = synth.normal((dm.S, dm.d), 1.0, 3, "pos")
+    w = synth.normal((dm.V, dm.d), 0.3, 3, "w")
+    phi = synth.phi_table(dm.S, dm.d, 3)
+    _, _, steps, recs = oracle.decode_block(dm.as_dict(), [L], phi, w, emb, pos, 0.0, dm.S,
+                                            trace=True, rule=oracle.RULE_LEFT_TO_RIGHT)
+    # gamma = 0 would commit everything at once under the confidence rule; here one per step
+    assert steps == dm.S
+    for t, r in enumerate(recs):
+        assert list(r["n_committed"]) == [1, 1]
+        assert np.array_equal(np.nonzero(r["committed"][0])[0], [t])
+        assert np.array_equal(np.nonzero(r["committed"][1])[0], [t])
+        assert np.array_equal(r["tokens"][:, t], r["pred"][:, t])
+
+
+# ----------------------------------------------------------------------------- cache growth
+
+def test_kv_append_extends_the_attention_context_by_the_block():
+    # attention over the grown cache equals a softmax written out here over
+    # (old context rows) ++ (appended block rows) ++ (block keys)
+    B, S, Hq, Hkv, D, Lmax = 2, 3, 4, 2, 16, 12
+    q = bf16_exact((B, S, Hq, D)); kb = bf16_exact((B, S, Hkv, D)); vb = bf16_exact((B, S, Hkv, D))
+    kc = bf16_exact((B, Hkv, Lmax, D)); vc = bf16_exact((B, Hkv, Lmax, D))
+    kn = bf16_exact((B, S, Hkv, D)); vn = bf16_exact((B, S, Hkv, D))
+    ctx = [5, 0]
+    k2, v2, ln, ovf = oracle.kv_append(kc, vc, ctx, kn, vn)
+    assert list(ln) == [8, 3] and not ovf.any()
+    o, _ = oracle.block_attention(q, kb, vb, k2, v2, ln)
+    G = Hq // Hkv
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            keys = np.concatenate([kc[b, g, :ctx[b]], kn[b, :, g], kb[b, :, g]])
+            vals = np.concatenate([vc[b, g, :ctx[b]], vn[b, :, g], vb[b, :, g]])
+            sc = q[b, :, h] @ keys.T / math.sqrt(D)
+            w = np.exp(sc - sc.max(axis=1, keepdims=True))
+            ref = (w / w.sum(axis=1, keepdims=True)) @ vals
+            assert np.allclose(o[b, :, h], ref, atol=1e-13)
+    # rows outside the appended window are untouched
+    assert np.array_equal(k2[0, :, :5], kc[0, :, :5]) and np.array_equal(k2[0, :, 8:], kc[0, :, 8:])
+
+
+def test_kv_append_overflow_leaves_the_sequence_unchanged():
+    B, S, Hkv, D, Lmax = 2, 4, 1, 8, 10
+    kc = bf16_exact((B, Hkv, Lmax, D)); vc = bf16_exact((B, Hkv, Lmax, D))
+    kn = bf16_exact((B, S, Hkv, D)); vn = bf16_exact((B, S, Hkv, D))
+    k2, v2, ln, ovf = oracle.kv_append(kc, vc, [7, 6], kn, vn)
+    assert list(ovf) == [True, False] and list(ln) == [7, 10]
+    assert np.array_equal(k2[0], kc[0]) and np.array_equal(v2[0], vc[0])
+    assert np.array_equal(k2[1, 0, 6:10], kn[1, :, 0])
