@@ -22,10 +22,13 @@ TD_FN_LMHEAD_COMMIT = 2
 TD_FN_DENOISE_STEP = 3
 TD_FN_DECODE_BLOCK = 4
 
+TD_COMMIT_CONFIDENCE = 0      # mask-diffusion: confidence masking with threshold gamma
+TD_COMMIT_LEFT_TO_RIGHT = 1   # mock-AR reading: one commit per step, lowest masked index
+
 # Every symbol the header declares (checked by the tests).
 EXPORTED = ("td_workspace_size", "td_status_string", "td_adaln_modulate", "td_block_attention",
             "td_lmhead_commit", "td_denoise_step", "td_decode_block", "td_device_error",
-            "td_lmhead_commit_static")
+            "td_lmhead_commit_static", "td_kv_append")
 
 
 class TdError(RuntimeError):
@@ -42,6 +45,10 @@ class td_dims(ctypes.Structure):
 class td_layer(ctypes.Structure):
     _fields_ = [("wqkv", ctypes.c_void_p), ("wo", ctypes.c_void_p), ("ada_E", ctypes.c_void_p),
                 ("k_ctx", ctypes.c_void_p), ("v_ctx", ctypes.c_void_p)]
+
+
+class td_kv(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -63,14 +70,16 @@ def lib() -> ctypes.CDLL:
         L.td_adaln_modulate.argtypes = [vp, vp, vp, i, i, f, vp, vp]
         L.td_block_attention.argtypes = [ctypes.POINTER(td_dims), vp, vp, vp, vp, vp, vp, vp, vp,
                                          vp, sz, vp]
-        L.td_lmhead_commit.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, vp, vp, vp, vp, vp,
-                                       vp, vp, sz, vp]
+        L.td_lmhead_commit.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, i, vp, vp, vp, vp,
+                                       vp, vp, vp, sz, vp]
         L.td_denoise_step.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer), vp, vp,
-                                      vp, vp, vp, vp, i, i, f, vp, vp, vp, vp, vp, vp, vp, sz,
-                                      vp]
+                                      vp, vp, vp, vp, i, i, f, i, vp, vp, vp, vp, vp, vp, vp,
+                                      sz, vp]
         L.td_decode_block.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer), vp, vp,
-                                      vp, vp, vp, i, i, f, vp, vp, vp, vp, vp, vp,
+                                      vp, vp, vp, i, i, f, i, vp, vp, vp, vp, vp, vp,
                                       ctypes.POINTER(i), vp, sz, vp]
+        L.td_kv_append.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer),
+                                   ctypes.POINTER(td_kv), vp, vp]
         L.td_device_error.argtypes = [ctypes.POINTER(i)]
         L.td_lmhead_commit_static.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, vp, vp, vp,
                                                vp, vp, vp, vp]
@@ -170,7 +179,8 @@ def _outs(B, S, device, conf, pred, n_committed, all_done):
 
 
 def td_lmhead_commit(dims, h, w_lm, gamma: float, force_all: bool, tokens, masked, conf=None,
-                     pred=None, n_committed=None, all_done=None, ws=None, stream=None):
+                     pred=None, n_committed=None, all_done=None, ws=None, stream=None,
+                     rule: int = TD_COMMIT_CONFIDENCE):
     """Updates tokens / masked in place; returns (conf, pred, n_committed, all_done)."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     conf, pred, n_committed, all_done = _outs(dm.B, dm.S, h.device, conf, pred, n_committed,
@@ -178,7 +188,8 @@ def td_lmhead_commit(dims, h, w_lm, gamma: float, force_all: bool, tokens, maske
     if ws is None:
         ws = workspace(dm, TD_FN_LMHEAD_COMMIT, h.device)
     _check("td_lmhead_commit",
-           lib().td_lmhead_commit(ctypes.byref(dm), _ptr(h), _ptr(w_lm), gamma, int(force_all),
+           lib().td_lmhead_commit(ctypes.byref(dm), _ptr(h), _ptr(w_lm), gamma, int(rule),
+                                  int(force_all),
                                   _ptr(tokens), _ptr(masked), _ptr(conf), _ptr(pred),
                                   _ptr(n_committed), _ptr(all_done), _ptr(ws), ws.numel(),
                                   _stream(stream)))
@@ -210,7 +221,8 @@ def _layers(layers: Sequence[Dict[str, torch.Tensor]]):
 
 def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tokens, masked,
                     h=None, emb=None, pos=None, ctx_len=None, conf=None, pred=None,
-                    n_committed=None, all_done=None, ws=None, stream=None):
+                    n_committed=None, all_done=None, ws=None, stream=None,
+                    rule: int = TD_COMMIT_CONFIDENCE):
     """One denoising step; tokens / masked updated in place.
     Returns (conf, pred, n_committed, all_done)."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
@@ -222,7 +234,8 @@ def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tok
     arr = _layers(layers)
     _check("td_denoise_step",
            lib().td_denoise_step(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(h), _ptr(emb),
-                                 _ptr(pos), _ptr(w_lm), _ptr(phi_t), t, T, gamma, _ptr(tokens),
+                                 _ptr(pos), _ptr(w_lm), _ptr(phi_t), t, T, gamma, int(rule),
+                                 _ptr(tokens),
                                  _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
                                  _ptr(all_done), _ptr(ws), ws.numel(), _stream(stream)))
     return conf, pred, n_committed, all_done
@@ -230,7 +243,8 @@ def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tok
 
 def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: float, tokens,
                     masked, t_start: int = 1, ctx_len=None, conf=None, pred=None,
-                    n_committed=None, all_done=None, ws=None, stream=None) -> int:
+                    n_committed=None, all_done=None, ws=None, stream=None,
+                    rule: int = TD_COMMIT_CONFIDENCE) -> int:
     """Runs the block decode loop in place on tokens / masked; returns the steps taken."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     dev = w_lm.device
@@ -242,8 +256,22 @@ def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: floa
     arr = _layers(layers)
     _check("td_decode_block",
            lib().td_decode_block(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(emb), _ptr(pos),
-                                 _ptr(w_lm), _ptr(phi_table), t_start, T, gamma, _ptr(tokens),
+                                 _ptr(w_lm), _ptr(phi_table), t_start, T, gamma, int(rule),
+                                 _ptr(tokens),
                                  _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
                                  _ptr(all_done), ctypes.byref(steps), _ptr(ws), ws.numel(),
                                  _stream(stream)))
     return steps.value
+
+
+def td_kv_append(dims, layers, block_kv, ctx_len, stream=None) -> None:
+    """Appends each layer's committed-block keys / values (block_kv: a list of (k, v) device
+    tensors [B, S, Hkv, D] bf16) to that layer's context cache at ctx_len, and grows
+    ctx_len [B] (int32, device) by S, on the device."""
+    dm = dims if isinstance(dims, td_dims) else dims_from(dims)
+    arr = _layers(layers)
+    kv = (td_kv * max(1, len(block_kv)))()
+    for i, (k, v) in enumerate(block_kv):
+        kv[i] = td_kv(_ptr(k), _ptr(v))
+    _check("td_kv_append", lib().td_kv_append(ctypes.byref(dm), arr, kv, _ptr(ctx_len),
+                                              _stream(stream)))

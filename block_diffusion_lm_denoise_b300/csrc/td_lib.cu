@@ -276,7 +276,8 @@ td_status launch_adaln(const void* h, const float* E, const float* phi, int rows
 // With row_pos / m_count set, h holds only the rows masked at the step start (compacted,
 // *m_count of them on the device) and the other rows are reported as not evaluated.
 td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, float gamma,
-                            int force_all, int* tokens, unsigned char* masked, float* conf,
+                            int rule, int force_all, int* tokens, unsigned char* masked,
+                            float* conf,
                             int* pred, int* n_committed, int* all_done, void* ws,
                             cudaStream_t st, int nsm, const int* skip = nullptr,
                             int* steps = nullptr, const int* row_pos = nullptr,
@@ -301,7 +302,8 @@ td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, 
   if (s != TD_OK) return s;
   TD_CUDA(cudaMemsetAsync(counters, 0, 2 * sizeof(int), st));
   merge_commit_kernel<<<dm->B, 32 * std::min(dm->S, 32), 0, st>>>(pmax, parg, psum, nt, dm->S, gamma,
-                                                         force_all, tokens, masked, conf, pred,
+                                                         force_all, rule, tokens, masked, conf,
+                                                         pred,
                                                          n_committed, all_done, counters,
                                                          skip, steps, row_pos);
   TD_CUDA(cudaGetLastError());
@@ -439,7 +441,8 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
 
 td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len, const void* h,
                    const void* emb, const void* pos, const void* w_lm, const float* phi_t,
-                   int t, int T, float gamma, int* tokens, unsigned char* masked, float* conf,
+                   int t, int T, float gamma, int rule, int* tokens, unsigned char* masked,
+                   float* conf,
                    int* pred, int* n_committed, int* all_done, void* ws, cudaStream_t st,
                    int nsm, const int* skip = nullptr, int* steps = nullptr) {
   const StepWs w = carve_step(dm, ws, nsm);
@@ -455,7 +458,9 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
   TD_CUDA(cudaGetLastError());
   // the LM head evaluates only the rows still masked now: the last layer writes them,
   // compacted, into h_lm
-  lm_rows_kernel<<<1, kRowsThreads, 0, st>>>(masked, M, w.row_pos, w.m_count, skip);
+  const int first_only = (rule == kRuleLeftToRight && t != T) ? 1 : 0;
+  lm_rows_kernel<<<1, kRowsThreads, 0, st>>>(masked, M, dm->S, first_only, w.row_pos,
+                                             w.m_count, skip);
   TD_CUDA(cudaGetLastError());
   const int nq = dm->Hq * dm->D, nk = dm->Hkv * dm->D;
   const int bn = M >= 512 ? 256 : 128;
@@ -483,7 +488,8 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
     gather_rows_kernel<<<M, 256, 0, st>>>(w.h, w.row_pos, w.h_lm, d, skip);
     TD_CUDA(cudaGetLastError());
   }
-  return run_lmhead_commit(dm, w.h_lm, w_lm, gamma, t == T ? 1 : 0, tokens, masked, conf, pred,
+  return run_lmhead_commit(dm, w.h_lm, w_lm, gamma, rule, t == T ? 1 : 0, tokens, masked, conf,
+                           pred,
                            n_committed, all_done, w.lm, st, nsm, skip, steps, w.row_pos,
                            w.m_count);
 }
@@ -553,10 +559,10 @@ cudaStream_t capture_stream() {
 // the caller then runs the host loop.
 td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx_len,
                        const void* emb, const void* pos, const void* w_lm,
-                       const float* phi_table, int t_start, int T, float gamma, int* tokens,
-                       unsigned char* masked, float* conf, int* pred, int* n_committed,
-                       int* all_done, void* ws, size_t ws_bytes, cudaStream_t st, int nsm,
-                       int* steps_taken, int* done) {
+                       const float* phi_table, int t_start, int T, float gamma, int rule,
+                       int* tokens, unsigned char* masked, float* conf, int* pred,
+                       int* n_committed, int* all_done, void* ws, size_t ws_bytes,
+                       cudaStream_t st, int nsm, int* steps_taken, int* done) {
   const StepWs w = carve_step(dm, ws, nsm);
   LoopKey key;
   int dev = 0;
@@ -568,6 +574,7 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
   uint32_t gbits;
   std::memcpy(&gbits, &gamma, 4);
   key.v.push_back(gbits);
+  key.v.push_back((uint64_t)rule);
   for (int l = 0; l < dm->n_layers; ++l) {
     u(layers[l].wqkv); u(layers[l].wo); u(layers[l].ada_E); u(layers[l].k_ctx); u(layers[l].v_ctx);
   }
@@ -593,8 +600,8 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
       s = TD_ERR_CUDA;
     for (int t = t_start; t <= T && s == TD_OK; ++t)
       s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
-                   phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, tokens, masked, conf,
-                   pred, n_committed, all_done, ws, cs, nsm, all_done, w.loop);
+                   phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, tokens, masked,
+                   conf, pred, n_committed, all_done, ws, cs, nsm, all_done, w.loop);
     cudaGraph_t g = nullptr;
     const cudaError_t ee = cudaStreamEndCapture(cs, &g);
     if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
@@ -629,6 +636,10 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
   *steps_taken = host[0];
   *done = host[1];
   return TD_OK;
+}
+
+bool rule_ok(int rule) {
+  return rule == TD_COMMIT_CONFIDENCE || rule == TD_COMMIT_LEFT_TO_RIGHT;
 }
 
 bool ws_ok(const void* ws, size_t have, size_t need) {
@@ -702,27 +713,29 @@ td_status td_block_attention(const td_dims* dims, const void* q, const void* k_b
 }
 
 td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm, float gamma,
-                           int force_all, int* tokens, unsigned char* masked, float* conf,
-                           int* pred, int* n_committed, int* all_done, void* ws, size_t ws_bytes,
-                           void* stream) {
+                           int rule, int force_all, int* tokens, unsigned char* masked,
+                           float* conf, int* pred, int* n_committed, int* all_done, void* ws,
+                           size_t ws_bytes, void* stream) {
   td_status s = check_lm_dims(dims);
   if (s != TD_OK) return s;
+  if (!rule_ok(rule)) return TD_ERR_INVALID_ARG;
   if (!h || !w_lm || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
     return TD_ERR_INVALID_ARG;
   if (std::isnan(gamma)) return TD_ERR_INVALID_ARG;
   if (!aligned16(h) || !aligned16(w_lm)) return TD_ERR_INVALID_ARG;
   if (!ws_ok(ws, ws_bytes, lm_ws_bytes(dims->B * dims->S, dims->V))) return TD_ERR_WORKSPACE;
-  return run_lmhead_commit(dims, h, w_lm, gamma, force_all, tokens, masked, conf, pred,
+  return run_lmhead_commit(dims, h, w_lm, gamma, rule, force_all, tokens, masked, conf, pred,
                            n_committed, all_done, ws, (cudaStream_t)stream, sm_count());
 }
 
 td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* h, const void* emb, const void* pos, const void* w_lm,
-                          const float* phi_t, int t, int T, float gamma, int* tokens,
+                          const float* phi_t, int t, int T, float gamma, int rule, int* tokens,
                           unsigned char* masked, float* conf, int* pred, int* n_committed,
                           int* all_done, void* ws, size_t ws_bytes, void* stream) {
   td_status s = check_dims(dims, true);
   if (s != TD_OK) return s;
+  if (!rule_ok(rule)) return TD_ERR_INVALID_ARG;
   if ((s = check_layers(dims, layers)) != TD_OK) return s;
   if (!w_lm || !phi_t || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
     return TD_ERR_INVALID_ARG;
@@ -730,18 +743,20 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
   if (t < 1 || T < 1 || t > T || std::isnan(gamma)) return TD_ERR_INVALID_ARG;
   const int nsm = sm_count();
   if (!ws_ok(ws, ws_bytes, carve_step(dims, nullptr, nsm).total)) return TD_ERR_WORKSPACE;
-  return run_step(dims, layers, ctx_len, h, emb, pos, w_lm, phi_t, t, T, gamma, tokens, masked,
+  return run_step(dims, layers, ctx_len, h, emb, pos, w_lm, phi_t, t, T, gamma, rule, tokens,
+                  masked,
                   conf, pred, n_committed, all_done, ws, (cudaStream_t)stream, nsm);
 }
 
 td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* emb, const void* pos, const void* w_lm,
-                          const float* phi_table, int t_start, int T, float gamma, int* tokens,
-                          unsigned char* masked, float* conf, int* pred, int* n_committed,
-                          int* all_done, int* steps_taken, void* ws, size_t ws_bytes,
-                          void* stream) {
+                          const float* phi_table, int t_start, int T, float gamma, int rule,
+                          int* tokens, unsigned char* masked, float* conf, int* pred,
+                          int* n_committed, int* all_done, int* steps_taken, void* ws,
+                          size_t ws_bytes, void* stream) {
   td_status s = check_dims(dims, true);
   if (s != TD_OK) return s;
+  if (!rule_ok(rule)) return TD_ERR_INVALID_ARG;
   if ((s = check_layers(dims, layers)) != TD_OK) return s;
   if (!emb || !pos || !w_lm || !phi_table || !tokens || !masked || !conf || !pred ||
       !n_committed || !all_done || !steps_taken)
@@ -762,8 +777,8 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   }
   int done = 0;
   if (t_start <= T) {
-    s = decode_graph(dims, layers, ctx_len, emb, pos, w_lm, phi_table, t_start, T, gamma, tokens,
-                     masked, conf, pred, n_committed, all_done, ws, ws_bytes, st, nsm,
+    s = decode_graph(dims, layers, ctx_len, emb, pos, w_lm, phi_table, t_start, T, gamma, rule,
+                     tokens, masked, conf, pred, n_committed, all_done, ws, ws_bytes, st, nsm,
                      steps_taken, &done);
     if (s == TD_OK) return done ? TD_OK : TD_ERR_NOT_CONVERGED;
     if (s != TD_ERR_UNSUPPORTED) return s;
@@ -772,8 +787,8 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   *steps_taken = 0;
   for (int t = t_start; t <= T; ++t) {
     s = run_step(dims, layers, ctx_len, nullptr, emb, pos, w_lm,
-                 phi_table + (size_t)(t - 1) * 6 * dims->d, t, T, gamma, tokens, masked, conf,
-                 pred, n_committed, all_done, ws, st, nsm);
+                 phi_table + (size_t)(t - 1) * 6 * dims->d, t, T, gamma, rule, tokens, masked,
+                 conf, pred, n_committed, all_done, ws, st, nsm);
     if (s != TD_OK) return s;
     TD_CUDA(cudaMemcpyAsync(&done, all_done, sizeof(int), cudaMemcpyDeviceToHost, st));
     TD_CUDA(cudaStreamSynchronize(st));
@@ -781,6 +796,39 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
     if (done) break;
   }
   return done ? TD_OK : TD_ERR_NOT_CONVERGED;
+}
+
+td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv* block_kv,
+                       int* ctx_len, void* stream) {
+  td_status s = check_dims(dims, false);
+  if (s != TD_OK) return s;
+  if (dims->n_layers < 0 || (dims->n_layers > 0 && (!layers || !block_kv)) || !ctx_len)
+    return TD_ERR_INVALID_ARG;
+  if (dims->Lmax < dims->S) return TD_ERR_INVALID_ARG;   // a block can never fit
+  for (int l = 0; l < dims->n_layers; ++l) {
+    const td_layer& L = layers[l];
+    const td_kv& N = block_kv[l];
+    if (!L.k_ctx || !L.v_ctx || !N.k || !N.v) return TD_ERR_INVALID_ARG;
+    if (!aligned16(L.k_ctx) || !aligned16(L.v_ctx) || !aligned16(N.k) || !aligned16(N.v))
+      return TD_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  const long long chunks = (long long)dims->B * dims->S * dims->Hkv * (dims->D / 8);
+  const int threads = 256;
+  const int blocks = (int)std::min<long long>((chunks + threads - 1) / threads, 4 * sm_count());
+  for (int l = 0; l < dims->n_layers; ++l) {
+    // the caches are written here: the const in td_layer is the attention's read-only view
+    kv_append_kernel<<<blocks, threads, 0, st>>>(
+        static_cast<const uint16_t*>(block_kv[l].k), static_cast<const uint16_t*>(block_kv[l].v),
+        static_cast<uint16_t*>(const_cast<void*>(layers[l].k_ctx)),
+        static_cast<uint16_t*>(const_cast<void*>(layers[l].v_ctx)), ctx_len, dims->B, dims->S,
+        dims->Hkv, dims->D, dims->Lmax);
+    TD_CUDA(cudaGetLastError());
+  }
+  kv_len_update_kernel<<<(dims->B + 255) / 256, 256, 0, st>>>(ctx_len, dims->B, dims->S,
+                                                              dims->Lmax);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
 }
 
 td_status td_device_error(int* code) {
@@ -844,6 +892,7 @@ extern "C" td_status td_lmhead_commit_static(const td_dims* dims, const void* h,
   void* ws = nullptr;
   if ((s = static_scratch_addr(&ws)) != TD_OK) return s;
   // run_lmhead_commit clears the commit counters in the scratch before the merge kernel.
-  return run_lmhead_commit(dims, h, w_lm, gamma, force_all, tokens, masked, conf, pred,
-                           n_committed, all_done, ws, (cudaStream_t)stream, sm_count());
+  return run_lmhead_commit(dims, h, w_lm, gamma, TD_COMMIT_CONFIDENCE, force_all, tokens,
+                           masked, conf, pred, n_committed, all_done, ws, (cudaStream_t)stream,
+                           sm_count());
 }

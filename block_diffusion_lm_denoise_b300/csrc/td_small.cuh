@@ -184,20 +184,33 @@ __global__ void __launch_bounds__(256)
 }
 
 // Rows the LM head evaluates in a denoise step: those still masked when the step starts
-// (committed rows need no logits). One CTA of kRowsThreads threads; thread t owns the
-// contiguous rows [t * per, (t + 1) * per). row_pos[r] = index of row r among the masked rows
-// (row order kept), or -1; *count = number of masked rows.
+// (committed rows need no logits); under the left-to-right rule before the last step, only
+// the lowest masked row of each sequence (the only one that can commit). One CTA of
+// kRowsThreads threads; thread t owns the contiguous rows [t * per, (t + 1) * per).
+// row_pos[r] = index of row r among the selected rows (row order kept), or -1;
+// *count = number of selected rows.
 constexpr int kRowsThreads = 1024;
+constexpr int kRuleConfidence = 0;
+constexpr int kRuleLeftToRight = 1;
+
+__device__ __forceinline__ bool lm_row_selected(const unsigned char* masked, int r, int S,
+                                                bool first_only) {
+  if (masked[r] == 0) return false;
+  if (!first_only) return true;
+  for (int j = r - r % S; j < r; ++j)
+    if (masked[j] != 0) return false;
+  return true;
+}
 
 __global__ void __launch_bounds__(kRowsThreads)
-    lm_rows_kernel(const unsigned char* __restrict__ masked, int M, int* __restrict__ row_pos,
-                   int* __restrict__ count, const int* skip) {
+    lm_rows_kernel(const unsigned char* __restrict__ masked, int M, int S, int first_only,
+                   int* __restrict__ row_pos, int* __restrict__ count, const int* skip) {
   if (skip != nullptr && *skip != 0) return;
   __shared__ int warp_tot[kRowsThreads / 32];
   const int per = (M + kRowsThreads - 1) / kRowsThreads;
   const int r0 = min(M, (int)threadIdx.x * per), r1 = min(M, r0 + per);
   int n = 0;
-  for (int r = r0; r < r1; ++r) n += masked[r] != 0;
+  for (int r = r0; r < r1; ++r) n += lm_row_selected(masked, r, S, first_only != 0);
   // exclusive scan of n over the block: within the warp, then over the warp totals
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = n;
@@ -219,7 +232,8 @@ __global__ void __launch_bounds__(kRowsThreads)
   }
   __syncthreads();
   int base = incl - n + (warp > 0 ? warp_tot[warp - 1] : 0);
-  for (int r = r0; r < r1; ++r) row_pos[r] = masked[r] != 0 ? base++ : -1;
+  for (int r = r0; r < r1; ++r)
+    row_pos[r] = lm_row_selected(masked, r, S, first_only != 0) ? base++ : -1;
   if (threadIdx.x == kRowsThreads - 1) *count = warp_tot[31];
 }
 
@@ -242,7 +256,8 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ h, const int* __
 __global__ void __launch_bounds__(1024)
     merge_commit_kernel(const float* __restrict__ part_max, const int* __restrict__ part_arg,
                         const float* __restrict__ part_sum, int n_tiles, int S, float gamma,
-                        int force_all, int* tokens, unsigned char* masked, float* conf_out,
+                        int force_all, int rule, int* tokens, unsigned char* masked,
+                        float* conf_out,
                         int* pred_out, int* n_committed, int* all_done, int* counters,
                         const int* skip, int* steps_taken, const int* row_pos) {
   // skip: the decode loop already finished; steps_taken (optional) counts the steps that ran;
@@ -327,6 +342,13 @@ __global__ void __launch_bounds__(1024)
     bool take[2] = {false, false};
     if (force_all) {
       take[0] = msk[0]; take[1] = msk[1];
+    } else if (rule == kRuleLeftToRight) {
+      // the lowest-index masked position, whatever its confidence
+      const unsigned m0 = __ballot_sync(0xffffffffu, msk[0]);
+      const unsigned m1 = __ballot_sync(0xffffffffu, msk[1]);
+      const int lo = m0 ? __ffs(m0) - 1 : (m1 ? 32 + __ffs(m1) - 1 : -1);
+      take[0] = (lane == lo);
+      take[1] = (lane + 32 == lo);
     } else if (any_thr) {
       take[0] = thr[0]; take[1] = thr[1];
     } else if (any_msk) {
@@ -378,6 +400,41 @@ __global__ void __launch_bounds__(1024)
       }
     }
   }
+}
+
+// Context-cache append: row ctx_len[b] + i of KV head g of a layer's cache receives
+// token i of head g of the block's keys / values ([B, S, Hkv, D], token-major). One thread
+// per 16-byte chunk; sequences whose cache would pass Lmax are skipped (flagged by the
+// length update below).
+__global__ void kv_append_kernel(const uint16_t* __restrict__ k_new,
+                                 const uint16_t* __restrict__ v_new, uint16_t* __restrict__ k_ctx,
+                                 uint16_t* __restrict__ v_ctx, const int* __restrict__ ctx_len,
+                                 int B, int S, int Hkv, int D, int Lmax) {
+  const int c16 = D / 8;
+  const long long total = (long long)B * S * Hkv * c16;
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+       x += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(x % c16);
+    long long row = x / c16;               // (b, i, g) of the block tensor
+    const int g = (int)(row % Hkv);
+    const int i = (int)((row / Hkv) % S);
+    const int b = (int)(row / ((long long)Hkv * S));
+    const int L = ctx_len[b];
+    if (L < 0 || L + S > Lmax) continue;
+    const size_t dst = (((size_t)b * Hkv + g) * Lmax + (size_t)(L + i)) * D + (size_t)c * 8;
+    const size_t src = (size_t)row * D + (size_t)c * 8;
+    *reinterpret_cast<uint4*>(k_ctx + dst) = *reinterpret_cast<const uint4*>(k_new + src);
+    *reinterpret_cast<uint4*>(v_ctx + dst) = *reinterpret_cast<const uint4*>(v_new + src);
+  }
+}
+
+// After every layer's append: ctx_len[b] += S, or the overflow is recorded.
+__global__ void kv_len_update_kernel(int* ctx_len, int B, int S, int Lmax) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int L = ctx_len[b];
+  if (L < 0 || L + S > Lmax) record_error(ERR_CTX_FULL);
+  else ctx_len[b] = L + S;
 }
 
 }  // namespace td

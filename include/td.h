@@ -76,6 +76,22 @@ typedef struct td_layer {
   const void* v_ctx;
 } td_layer;
 
+/* Commit rule of a step (the pages name three inference modes of one checkpoint:
+ * mask-diffusion, mock-AR and AR-only; [chathome] modes paragraph, [aiboss] overview).
+ *   TD_COMMIT_CONFIDENCE    mask-diffusion: confidence masking with threshold gamma
+ *                           ([chathome] evaluation paragraph), fallback to the single most
+ *                           confident masked position (lowest index on ties).
+ *   TD_COMMIT_LEFT_TO_RIGHT mock-AR, a reading (the pages do not define the mode): exactly
+ *                           one commit per step, the lowest-index masked position whatever its
+ *                           confidence, as AR decoding commits one token per step in order
+ *                           ([chathome] generation paragraph). gamma is not used.
+ * Both commit every masked position at the last step (force_all / t == T). AR-only mode runs
+ * the context tower alone and is outside this library. */
+typedef enum td_commit_rule {
+  TD_COMMIT_CONFIDENCE = 0,
+  TD_COMMIT_LEFT_TO_RIGHT = 1
+} td_commit_rule;
+
 /* Selector for td_workspace_size(). */
 enum {
   TD_FN_ADALN_MODULATE = 0,
@@ -128,18 +144,20 @@ td_status td_block_attention(const td_dims* dims, const void* q, const void* k_b
  * For every row r = b*S + i:  z = h_r . W_lm^T (fp32 accumulate, never stored),
  *   conf[r] = max_v softmax(z)_v = 1 / sum_v exp(z_v - max z),
  *   pred[r] = the lowest v with z_v = max z.
- * Commit, per sequence b: C = { i : masked[b,i] && conf >= gamma }; if C is empty and some
- * position is masked, C = { the lowest-index masked i of maximal conf }; if force_all,
+ * Commit, per sequence b, rule TD_COMMIT_CONFIDENCE: C = { i : masked[b,i] && conf >= gamma };
+ * if C is empty and some position is masked, C = { the lowest-index masked i of maximal
+ * conf }. Rule TD_COMMIT_LEFT_TO_RIGHT: C = { the lowest-index masked i }. If force_all,
  * C = every masked i. For i in C: tokens[b,i] = pred, masked[b,i] = 0.
  * n_committed[b] = |C|; *all_done = 1 if no position of any sequence is still masked.
  *   h     bf16 [B*S, d]           w_lm bf16 [V, d]
  *   tokens int32 [B, S] in/out    masked uint8 [B, S] in/out (1 = still [MASK])
  *   conf  fp32 [B, S] out (every row)   pred int32 [B, S] out (every row)
  *   n_committed int32 [B] out           all_done int32 [1] out
+ *   rule  a td_commit_rule (anything else: TD_ERR_INVALID_ARG)
  * Only B, S, d, V of dims are read. Committed positions are never rewritten. */
 td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm, float gamma,
-                           int force_all, int* tokens, unsigned char* masked, float* conf,
-                           int* pred, int* n_committed, int* all_done, void* ws,
+                           int rule, int force_all, int* tokens, unsigned char* masked,
+                           float* conf, int* pred, int* n_committed, int* all_done, void* ws,
                            size_t ws_bytes, void* stream);
 
 /* One denoising step of the denoiser tower over the block ([chathome] inference and
@@ -150,16 +168,17 @@ td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm,
  *   m = E_l + phi_t; x_mod = adaLN(h) as in td_adaln_modulate (eps = 1e-6);
  *   [q | k | v] = bf16(x_mod . wqkv^T); o = td_block_attention(...);
  *   h = bf16(h + m[2] * (o . wo^T))            (m[2] is the gate)
- * and finally td_lmhead_commit with force_all = (t == T), evaluated only on the rows that
- * are masked when the step starts (committed rows need no logits; the last layer writes just
- * those rows, compacted, and the LM head reads their count on the device). Rows already
- * committed when the step starts get conf = 0 and pred = -1.
+ * and finally td_lmhead_commit with the given rule and force_all = (t == T), evaluated only
+ * on the rows that can commit: those masked when the step starts, and under
+ * TD_COMMIT_LEFT_TO_RIGHT before step T only the lowest masked row of each sequence
+ * (committed rows need no logits; the last layer writes just those rows, compacted, and the
+ * LM head reads their count on the device). Rows not evaluated get conf = 0 and pred = -1.
  *   phi_t fp32 [6, d]: the shared adaLN-single timestep vector of step t (1 <= t <= T).
  *   layers: HOST array of dims->n_layers td_layer structs (device pointers inside).
  *   ctx_len int32 [B] device or NULL.  Other outputs as in td_lmhead_commit. */
 td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* h, const void* emb, const void* pos, const void* w_lm,
-                          const float* phi_t, int t, int T, float gamma, int* tokens,
+                          const float* phi_t, int t, int T, float gamma, int rule, int* tokens,
                           unsigned char* masked, float* conf, int* pred, int* n_committed,
                           int* all_done, void* ws, size_t ws_bytes, void* stream);
 
@@ -178,10 +197,32 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
  * happen with force-commit at t == T; kept for callers that stop early). */
 td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* emb, const void* pos, const void* w_lm,
-                          const float* phi_table, int t_start, int T, float gamma, int* tokens,
-                          unsigned char* masked, float* conf, int* pred, int* n_committed,
-                          int* all_done, int* steps_taken, void* ws, size_t ws_bytes,
-                          void* stream);
+                          const float* phi_table, int t_start, int T, float gamma, int rule,
+                          int* tokens, unsigned char* masked, float* conf, int* pred,
+                          int* n_committed, int* all_done, int* steps_taken, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* The committed block's keys / values of one context-tower layer (the context tower's
+ * forward pass itself is outside this library; its output is the input here).
+ *   k, v  bf16 [B, S, Hkv, D] device, token-major */
+typedef struct td_kv {
+  const void* k;
+  const void* v;
+} td_kv;
+
+/* Context-cache growth after a block commits ([chathome] generation paragraph: once a block
+ * is committed the context tower takes it in, and the next block attends to it). For every
+ * layer l, sequence b, block position i and KV head g:
+ *   layers[l].k_ctx[b, g, ctx_len[b] + i, :] = block_kv[l].k[b, i, g, :]   (same for v)
+ * then ctx_len[b] += S. The caches named by layers (k_ctx, v_ctx) are WRITTEN.
+ *   block_kv: HOST array of dims->n_layers td_kv (device pointers inside).
+ *   ctx_len  int32 [B] device, in/out.
+ * A sequence whose cache would pass Lmax (or whose ctx_len is negative) is left unchanged
+ * and the device error word reads ERR_CTX_FULL (0x600, see td_device_error).
+ * Only B, S, Hkv, D, Lmax, n_layers of dims are read. Errors: TD_ERR_INVALID_ARG (null or
+ * misaligned pointers, Lmax < S). Asynchronous on stream; no workspace. */
+td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv* block_kv,
+                       int* ctx_len, void* stream);
 
 /* Reads and clears the device error word that bounded waits write (0 = none); the
  * current device is used. Synchronises the device. Returns TD_ERR_CUDA if the read fails. */
@@ -192,7 +233,7 @@ td_status td_device_error(int* code);
  * a plugin running inside a host framework whose device memory is owned by that framework's
  * own pool or budget, or a latency-bound loop that must never call cudaMalloc / cudaFree
  * (both may synchronise the device). Same arguments, semantics and results as
- * td_lmhead_commit, minus ws / ws_bytes.
+ * td_lmhead_commit with rule TD_COMMIT_CONFIDENCE, minus rule, ws and ws_bytes.
  * Scratch: a fixed 16 MiB array in device memory that is part of this library, so every GPU
  * that loads the library holds it until the process exits. Its device address is looked up
  * on the first call made on each device (with that device current); make that first call

@@ -59,13 +59,14 @@ def test_null_pointers_are_rejected_before_any_launch(lib):
     # every pointer null: validation must fail first
     assert lib.td_block_attention(ctypes.byref(dm), None, None, None, None, None, None, None,
                                   None, None, 0, None) == 1
-    assert lib.td_lmhead_commit(ctypes.byref(dm), None, None, 0.8, 0, None, None, None, None,
+    assert lib.td_lmhead_commit(ctypes.byref(dm), None, None, 0.8, 0, 0, None, None, None, None,
                                 None, None, None, 0, None) == 1
     assert lib.td_adaln_modulate(None, None, None, 4, 256, 1e-6, None, None) == 1
     steps = ctypes.c_int(0)
     assert lib.td_decode_block(ctypes.byref(dm), None, None, None, None, None, None, 1, 16,
-                               0.8, None, None, None, None, None, None, ctypes.byref(steps),
+                               0.8, 0, None, None, None, None, None, None, ctypes.byref(steps),
                                None, 0, None) == 1
+    assert lib.td_kv_append(ctypes.byref(dm), None, None, None, None) == 1
     # shapes outside the kernels' limits
     bad = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=80, V=1024, Lmax=64, n_layers=1)
     fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the shape check fails first
@@ -79,3 +80,10 @@ def test_undersized_workspace_is_rejected(lib):
     fake = ctypes.c_void_p(1 << 40)
     assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None, fake,
                                   None, fake, 16, None) == 2
+
+
+def test_unknown_commit_rule_is_rejected(lib):
+    dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=1)
+    fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the rule check fails first
+    assert lib.td_lmhead_commit(ctypes.byref(dm), fake, fake, 0.8, 7, 0, fake, fake, fake, fake,
+                                fake, fake, fake, 1 << 30, None) == 1

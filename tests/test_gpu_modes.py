@@ -1,0 +1,194 @@
+"""GPU parity of the mode variants and of multi-block generation against the fp64 oracle:
+the left-to-right commit rule (the mock-AR reading), the context-cache append, and several
+blocks decoded in a row with the cache growing between them."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_diffusion_lm_denoise_b300 as td
+import oracle
+from block_diffusion_lm_denoise_b300 import synth
+from parity_util import STACKED_CONF_BAND, compare_commit, first_masked, runner_up_ties
+
+pytestmark = pytest.mark.gpu
+
+L2R = td.TD_COMMIT_LEFT_TO_RIGHT
+
+
+def _np(t):
+    return oracle.as_f64(t)
+
+
+def test_lmhead_left_to_right_commits_the_lowest_masked_position(cuda_device):
+    M, S, V, d = 64, 16, 2048, 256
+    h = synth.normal((M, d), 1.0, 31, "h", cuda_device)
+    w = synth.normal((V, d), 0.3, 31, "w", cuda_device)
+    B = M // S
+    masked = synth.bernoulli((B, S), 0.6, 31, "m", cuda_device).to(torch.uint8)
+    masked[0] = 0                                   # a finished sequence stays untouched
+    tokens = torch.where(masked.bool(), torch.full((B, S), V, dtype=torch.int32, device=cuda_device),
+                         synth.integers((B, S), V, 31, "t", cuda_device))
+    t0, m0 = tokens.clone(), masked.clone()
+    dims = td.make_dims(B=B, S=S, d=d, Hq=1, Hkv=1, D=64, V=V, Lmax=0, n_layers=0)
+    conf, pred, ncom, done = td.td_lmhead_commit(dims, h, w, 0.0, False, tokens, masked, rule=L2R)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    c, p, gap, _ = oracle.lmhead_confidence(h, w)
+    tok_ref, msk_ref, n_ref, _ = oracle.commit(c.reshape(B, S), p.reshape(B, S), t0.cpu().numpy(),
+                                               m0.cpu().numpy().astype(bool), 0.0, False,
+                                               rule=oracle.RULE_LEFT_TO_RIGHT)
+    compare_commit(dict(conf=c.reshape(B, S), pred=p.reshape(B, S), gap=gap.reshape(B, S),
+                        tokens=tok_ref, masked=msk_ref),
+                   dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                        tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
+                   m0.cpu().numpy(), 0.0)
+    assert list(ncom.cpu().numpy()) == list(n_ref) and n_ref[0] == 0 and (n_ref[1:] == 1).all()
+
+
+def _small_model(seed, dm, cuda_device, w_scale=0.05):
+    layers = [synth._layer(seed, l, dm, 1 / math.sqrt(dm.d), 1 / math.sqrt(dm.Hq * dm.D), 1.0,
+                           cuda_device) for l in range(dm.n_layers)]
+    w_lm = synth.normal((dm.V, dm.d), w_scale, seed, "w_lm", cuda_device)
+    emb = synth.normal((dm.V + 1, dm.d), 1.0, seed, "emb", cuda_device)
+    pos = synth.normal((dm.S, dm.d), 1.0, seed, "pos", cuda_device)
+    phi = synth.phi_table(dm.S, dm.d, seed, cuda_device)
+    return layers, w_lm, emb, pos, phi
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_denoise_step_left_to_right_evaluates_one_row_per_sequence(cuda_device, D):
+    dm = synth.Dims(B=3, S=16, d=256, Hq=8, Hkv=2, D=D, V=1024, Lmax=100, n_layers=2)
+    layers, w_lm, emb, pos, phi = _small_model(41, dm, cuda_device)
+    masked = synth.bernoulli((dm.B, dm.S), 0.5, 41, "m", cuda_device).to(torch.uint8)
+    masked[1] = 0
+    tokens = torch.where(masked.bool(), torch.full((dm.B, dm.S), dm.V, dtype=torch.int32,
+                                                   device=cuda_device),
+                         synth.integers((dm.B, dm.S), dm.V, 41, "tok", cuda_device))
+    ctx = torch.tensor([100, 37, 0], dtype=torch.int32, device=cuda_device)
+    t0, m0 = tokens.clone(), masked.clone()
+    conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[4], 5, 16, 0.8,
+                                                tokens, masked, emb=emb, pos=pos, ctx_len=ctx,
+                                                rule=L2R)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    r = oracle.denoise_step(dm.as_dict(), layers, phi[4], w_lm, t0.cpu().numpy(),
+                            m0.cpu().numpy().astype(bool), 0.8, 5, 16, emb=emb, pos=pos,
+                            ctx_len=[100, 37, 0], rule=oracle.RULE_LEFT_TO_RIGHT)
+    m0n = m0.cpu().numpy().astype(bool)
+    compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                           tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
+                   m0n, 0.8, step=True, evaluated=first_masked(m0n))
+    assert list(ncom.cpu().numpy()) == [int(m0n[b].any()) for b in range(dm.B)]
+
+
+def test_decode_block_left_to_right_takes_s_steps_in_order(cuda_device):
+    dm = synth.Dims(B=2, S=8, d=256, Hq=8, Hkv=2, D=128, V=1024, Lmax=130, n_layers=2)
+    layers, w_lm, emb, pos, phi = _small_model(43, dm, cuda_device)
+    tokens = torch.full((dm.B, dm.S), dm.V, dtype=torch.int32, device=cuda_device)
+    masked = torch.ones((dm.B, dm.S), dtype=torch.uint8, device=cuda_device)
+    steps = td.td_decode_block(dm.as_dict(), layers, emb, pos, w_lm, phi, dm.S, 0.0, tokens,
+                               masked, rule=L2R)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    assert steps == dm.S and not masked.any()
+    tok_ref, msk_ref, steps_ref, recs = oracle.decode_block(
+        dm.as_dict(), [{k: v.cpu() for k, v in L.items()} for L in layers], phi.cpu(),
+        w_lm.cpu(), emb.cpu(), pos.cpu(), 0.0, dm.S, trace=True, rule=oracle.RULE_LEFT_TO_RIGHT)
+    assert steps_ref == dm.S
+    # ids are compared up to the first step whose committed position has a near-tie argmax
+    # (top-2 logit gap under 1e-4): from there on the two runs may legitimately differ
+    got = tokens.cpu().numpy()
+    for t, rec in enumerate(recs):
+        if (rec["gap"][:, t] < 1e-4).any():
+            break
+        assert np.array_equal(got[:, t], tok_ref[:, t]), t
+
+
+def test_kv_append_matches_oracle_and_flags_overflow(cuda_device):
+    B, S, Hkv, D, Lmax, n_layers = 3, 16, 2, 128, 70, 2
+    dm = td.make_dims(B=B, S=S, d=256, Hq=8, Hkv=Hkv, D=D, V=64, Lmax=Lmax, n_layers=n_layers)
+    layers, new = [], []
+    for l in range(n_layers):
+        layers.append(dict(wqkv=torch.zeros(16, dtype=torch.bfloat16, device=cuda_device),
+                           wo=torch.zeros(16, dtype=torch.bfloat16, device=cuda_device),
+                           ada_E=torch.zeros(16, device=cuda_device),
+                           k_ctx=synth.normal((B, Hkv, Lmax, D), 1.0, 51, f"k{l}", cuda_device),
+                           v_ctx=synth.normal((B, Hkv, Lmax, D), 1.0, 51, f"v{l}", cuda_device)))
+        new.append((synth.normal((B, S, Hkv, D), 1.0, 51, f"kn{l}", cuda_device),
+                    synth.normal((B, S, Hkv, D), 1.0, 51, f"vn{l}", cuda_device)))
+    start = [20, 54, 60]          # the last one would pass Lmax = 70
+    ctx = torch.tensor(start, dtype=torch.int32, device=cuda_device)
+    before = [(L["k_ctx"].clone(), L["v_ctx"].clone()) for L in layers]
+    td.td_kv_append(dm, layers, new, ctx)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0x600
+    for l in range(n_layers):
+        k2, v2, ln, ovf = oracle.kv_append(before[l][0], before[l][1], start, new[l][0], new[l][1])
+        assert np.array_equal(_np(layers[l]["k_ctx"]), k2)
+        assert np.array_equal(_np(layers[l]["v_ctx"]), v2)
+        assert list(ovf) == [False, False, True]
+    assert ctx.cpu().tolist() == [36, 70, 60]
+
+
+def test_three_blocks_with_the_cache_growing_between_them(cuda_device):
+    # multi-block generation: decode a block, append the context tower's keys / values of the
+    # committed block (a seeded per-token stand-in for that tower), decode the next block.
+    # Every step is compared with the oracle fed the GPU's state before that step, so a
+    # near-tie decision (excluded by the shared rules) cannot hide later mismatches.
+    dm = synth.Dims(B=3, S=16, d=256, Hq=8, Hkv=2, D=128, V=2048, Lmax=90 + 3 * 16,
+                    n_layers=2)
+    layers, w_lm, emb, pos, phi = _small_model(61, dm, cuda_device, w_scale=0.08)
+    # stand-in context tower: per layer a table token -> (k, v) rows [V + 1, Hkv, D]
+    ktab = [synth.normal((dm.V + 1, dm.Hkv, dm.D), 1.0, 61, f"ktab{l}", cuda_device)
+            for l in range(dm.n_layers)]
+    vtab = [synth.normal((dm.V + 1, dm.Hkv, dm.D), 1.0, 61, f"vtab{l}", cuda_device)
+            for l in range(dm.n_layers)]
+    ctx = torch.tensor([90, 12, 0], dtype=torch.int32, device=cuda_device)
+    cpu_layers = [{k: v.cpu() for k, v in L.items()} for L in layers]
+    ctx_ref = [90, 12, 0]
+    ws = td.workspace(dm.as_dict(), td.TD_FN_DECODE_BLOCK, cuda_device)
+    for blk in range(3):
+        tokens = torch.full((dm.B, dm.S), dm.V, dtype=torch.int32, device=cuda_device)
+        masked = torch.ones((dm.B, dm.S), dtype=torch.uint8, device=cuda_device)
+        # step by step through td_denoise_step, each step checked against the oracle
+        tk, mk = tokens.clone(), masked.clone()
+        for t in range(1, dm.S + 1):
+            t_before, m_before = tk.cpu().numpy(), mk.cpu().numpy().astype(bool)
+            conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[t - 1],
+                                                        t, dm.S, 0.8, tk, mk, emb=emb, pos=pos,
+                                                        ctx_len=ctx, ws=ws)
+            r = oracle.denoise_step(dm.as_dict(), cpu_layers, phi[t - 1].cpu(), w_lm.cpu(),
+                                    t_before, m_before, 0.8, t, dm.S, emb=emb.cpu(),
+                                    pos=pos.cpu(), ctx_len=ctx_ref)
+            ties = runner_up_ties(r["h_final"], w_lm.cpu(), pred.cpu().numpy(), r["pred"],
+                                  r["gap"], m_before)
+            compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                                   tokens=tk.cpu().numpy(), masked=mk.cpu().numpy()),
+                           m_before, 0.8, step=True, tie_extra=ties,
+                           conf_band=STACKED_CONF_BAND)
+            if int(done.item()):
+                break
+        # the loop entry point reproduces the step-by-step run bit for bit
+        steps = td.td_decode_block(dm.as_dict(), layers, emb, pos, w_lm, phi, dm.S, 0.8, tokens,
+                                   masked, ctx_len=ctx, ws=ws)
+        torch.cuda.synchronize()
+        assert td.td_device_error() == 0 and not masked.any() and steps == t
+        assert torch.equal(tokens, tk), blk
+        # grow the caches with the committed block (the same tokens on both sides)
+        tok = tokens.long()
+        new = [(ktab[l][tok].contiguous(), vtab[l][tok].contiguous()) for l in range(dm.n_layers)]
+        td.td_kv_append(dm.as_dict(), layers, new, ctx)
+        torch.cuda.synchronize()
+        assert td.td_device_error() == 0
+        for l in range(dm.n_layers):
+            k2, v2, ln, ovf = oracle.kv_append(cpu_layers[l]["k_ctx"], cpu_layers[l]["v_ctx"],
+                                               ctx_ref, new[l][0], new[l][1])
+            assert np.array_equal(_np(layers[l]["k_ctx"]), k2)
+            assert np.array_equal(_np(layers[l]["v_ctx"]), v2)
+            cpu_layers[l]["k_ctx"] = torch.from_numpy(k2).to(torch.bfloat16)
+            cpu_layers[l]["v_ctx"] = torch.from_numpy(v2).to(torch.bfloat16)
+        ctx_ref = [c + dm.S for c in ctx_ref]
+        assert ctx.cpu().tolist() == ctx_ref
