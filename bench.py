@@ -225,8 +225,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["attention", "lmhead"],
-                    help="launch one kernel family alone (for profiler captures)")
+    ap.add_argument("--only", choices=["attention", "lmhead", "step"],
+                    help="launch one kernel family alone, or one denoise step of one layer "
+                         "(for profiler captures)")
     ap.add_argument("--B", type=int, default=32)
     ap.add_argument("--L", type=int, default=8192)
     ap.add_argument("--M", type=int, default=1024)
@@ -285,6 +286,30 @@ def main():
     total_steps = sum(steps_taken)
     value = world * M * args.steps / (ms_max / 1e3)
     denoised = world * M * total_steps / (ms_max / 1e3)
+
+    # ---------------------------------------------------------------- commit-rule sweep
+    # steps per block and committed tokens/s of one block at other thresholds and under the
+    # left-to-right rule (the pages: lower gamma commits more per step; mock-AR one per step)
+    sweep = []
+    for g, rule in ((0.5 / dm.V, td.TD_COMMIT_CONFIDENCE), (0.5, td.TD_COMMIT_CONFIDENCE),
+                    (0.8, td.TD_COMMIT_CONFIDENCE), (0.95, td.TD_COMMIT_CONFIDENCE),
+                    (0.8, td.TD_COMMIT_LEFT_TO_RIGHT)):
+        def blk():
+            tokens.fill_(dm.V)
+            masked.fill_(1)
+            return td.td_decode_block(dims, wl.layers, wl.emb, wl.pos, wl.w_lm, wl.phi_table,
+                                      wl.T, g, tokens, masked, conf=outs[0], pred=outs[1],
+                                      n_committed=outs[2], all_done=outs[3], ws=ws, rule=rule)
+        blk()   # captures this argument set's graph
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        st = blk()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        bms = s0.elapsed_time(s1)
+        sweep.append({"gamma": g, "rule": "left_to_right" if rule else "confidence",
+                      "steps_per_block": st, "commits_per_step": round(M / st, 2),
+                      "committed_tokens_per_s": round(world * M / (bms / 1e3), 1)})
 
     # ---------------------------------------------------------------- end to end (host buffers)
     tok_h = torch.full((dm.B, dm.S), dm.V, dtype=torch.int32).pin_memory()
@@ -382,6 +407,7 @@ def main():
                        l2="inputs larger than L2 (3.2 GB of context KV + 1 GB LM head per step)"),
         "denoised_tokens_per_s": round(denoised, 1),
         "denoise_steps_per_block": round(total_steps / args.steps, 3),
+        "commit_sweep": sweep,
         "gpu_launches": launches_per_step * total_steps,
         "clocks": clocks.summary(),
         "roofline": dominant,
@@ -416,6 +442,24 @@ def run_only(args):
         for _ in range(args.reps):
             td.td_block_attention(dims, lay["q"], lay["k_blk"], lay["v_blk"], lay["k_ctx"],
                                   lay["v_ctx"], o=o, ws=ws)
+    elif args.only == "step":
+        # one denoise step of one layer at the decode-loop widths (d 4096, 32/2 heads, V
+        # 131072) with B sequences of context L: every kernel of a step, small on the device
+        from block_diffusion_lm_denoise_b300.synth import Dims, _layer, normal, phi_table
+        import math
+        dm = Dims(B=args.B, S=16, d=4096, Hq=32, Hkv=2, D=128, V=131072, Lmax=args.L,
+                  n_layers=1)
+        layers = [_layer(7, 0, dm, 1 / math.sqrt(dm.d), 1 / math.sqrt(dm.Hq * dm.D), 1.0, dev)]
+        w_lm = normal((dm.V, dm.d), 0.02, 7, "w_lm", dev)
+        emb = normal((dm.V + 1, dm.d), 1.0, 7, "emb", dev)
+        pos = normal((dm.S, dm.d), 1.0, 7, "pos", dev)
+        phi = phi_table(16, dm.d, 7, dev)
+        ws = td.workspace(dm.as_dict(), td.TD_FN_DENOISE_STEP, dev)
+        for _ in range(args.reps):
+            tokens = torch.full((dm.B, dm.S), dm.V, dtype=torch.int32, device=dev)
+            masked = torch.ones((dm.B, dm.S), dtype=torch.uint8, device=dev)
+            td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[0], 1, 16, 0.8, tokens, masked,
+                               emb=emb, pos=pos, ws=ws)
     else:
         wl = synth.lmhead_sweep(args.M, 16, 0.8, dev)
         dims = wl.dims.as_dict()
