@@ -13,6 +13,7 @@ from .td_oracle import (  # noqa: F401
     as_f64,
     bf16_round,
     block_attention,
+    block_positions,
     commit,
     decode_block,
     denoise_step,
@@ -23,4 +24,5 @@ from .td_oracle import (  # noqa: F401
     lmhead_confidence,
     oproj_gated_residual,
     qkv_project,
+    rope_rotate,
 )

@@ -32,8 +32,10 @@ notes of the repository):
   R2 one joint softmax per query row over context keys and block keys; no mask (the cache
      holds only past tokens; the block is bidirectional); the cached K/V are used as-is.
   R3 GQA groups are consecutive: query head h reads KV head h // (Hq / Hkv).
-  R4 no positional rotation; the decode loop adds a synthetic position table to the
-     embedding as a stand-in for the order information of the out-of-scope Mamba layers.
+  R4 no positional rotation by default; the decode loop adds a synthetic position table to
+     the embedding as a stand-in for the order information of the out-of-scope Mamba layers.
+     A rotary variant (rope_theta > 0) rotates the block's q and k at their absolute
+     positions ctx_len + i, interleaved pairs, before their bf16 rounding.
   R5 [MASK] is token id V, outside the LM head's V outputs.
   R6 conf = max softmax probability; pred = lowest id among the maxima; commit set
      {masked i : conf_i >= gamma}; if empty while something is masked, the lowest-index
@@ -108,18 +110,45 @@ def adaln_modulate(h, E, phi) -> np.ndarray:
 # Projections
 # ----------------------------------------------------------------------------------------
 
-def qkv_project(x_mod, wqkv, Hq: int, Hkv: int, D: int):
+def rope_rotate(x, positions, theta: float) -> np.ndarray:
+    """Rotary position embedding (a variant; the pages define no positional scheme, R4).
+
+    x [rows, heads, D] fp64; positions [rows]. Interleaved pairs: for j < D/2 the pair
+    (x[2j], x[2j+1]) is rotated by the angle pos * theta**(-2j/D):
+      x'[2j]   = x[2j] cos a - x[2j+1] sin a
+      x'[2j+1] = x[2j] sin a + x[2j+1] cos a
+    """
+    x = as_f64(x)
+    D = x.shape[-1]
+    j = np.arange(D // 2, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * j / D)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]   # [rows, D/2]
+    c = np.cos(ang)[:, None, :]
+    sn = np.sin(ang)[:, None, :]
+    x0 = x[..., 0::2]
+    x1 = x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * sn
+    out[..., 1::2] = x0 * sn + x1 * c
+    return out
+
+
+def qkv_project(x_mod, wqkv, Hq: int, Hkv: int, D: int, rope_pos=None, rope_theta: float = 0.0):
     """[q | k | v] = bf16(x_mod W_qkv), with W_qkv stored transposed as [(Hq+2Hkv)D, d].
 
-    Returns q [rows, Hq, D], k [rows, Hkv, D], v [rows, Hkv, D] (fp64 holding bf16 values,
-    storage point Q2).
+    With rope_theta > 0, q and k are rotated (rope_rotate, positions rope_pos [rows]) before
+    the rounding. Returns q [rows, Hq, D], k [rows, Hkv, D], v [rows, Hkv, D] (fp64 holding
+    bf16 values, storage point Q2).
     """
-    y = bf16_round(as_f64(x_mod) @ as_f64(wqkv).T)
+    y = as_f64(x_mod) @ as_f64(wqkv).T
     rows = y.shape[0]
     q = y[:, : Hq * D].reshape(rows, Hq, D)
     k = y[:, Hq * D: (Hq + Hkv) * D].reshape(rows, Hkv, D)
     v = y[:, (Hq + Hkv) * D: (Hq + 2 * Hkv) * D].reshape(rows, Hkv, D)
-    return q, k, v
+    if rope_theta > 0:
+        q = rope_rotate(q, rope_pos, rope_theta)
+        k = rope_rotate(k, rope_pos, rope_theta)
+    return bf16_round(q), bf16_round(k), bf16_round(v)
 
 
 def oproj_gated_residual(h, o, wo, gate) -> np.ndarray:
@@ -270,16 +299,27 @@ def embed(tokens, emb, pos) -> np.ndarray:
     return bf16_round(e + p)
 
 
-def layer_forward(h, layer, phi, dims, ctx_len=None):
+def block_positions(dims, ctx_len=None) -> np.ndarray:
+    """Absolute position of every block row b*S + i: ctx_len[b] + i (the block follows the
+    context; default ctx_len = Lmax)."""
+    B, S = dims["B"], dims["S"]
+    L = np.full(B, dims["Lmax"]) if ctx_len is None else np.asarray(ctx_len)
+    return (L[:, None] + np.arange(S)[None, :]).reshape(-1)
+
+
+def layer_forward(h, layer, phi, dims, ctx_len=None, rope_theta: float = 0.0):
     """One denoiser attention layer on the block hidden state h [B*S, d] (bf16 values).
 
     layer: dict with wqkv, wo, ada_E, k_ctx, v_ctx (tensors or arrays; k_ctx/v_ctx may hold
-    only the sequences in this call). Returns the new h and the attention output o.
+    only the sequences in this call). rope_theta > 0 rotates the block's q and k at their
+    absolute positions (the cached context keys are taken as already rotated by the context
+    tower). Returns the new h and the attention output o.
     """
     B, S, Hq, Hkv, D = dims["B"], dims["S"], dims["Hq"], dims["Hkv"], dims["D"]
     _, _, gate = adaln_vectors(layer["ada_E"], phi)
     x_mod = adaln_modulate(h, layer["ada_E"], phi)
-    q, k, v = qkv_project(x_mod, layer["wqkv"], Hq, Hkv, D)
+    q, k, v = qkv_project(x_mod, layer["wqkv"], Hq, Hkv, D,
+                          rope_pos=block_positions(dims, ctx_len), rope_theta=rope_theta)
     o, _ = block_attention(q.reshape(B, S, Hq, D), k.reshape(B, S, Hkv, D),
                            v.reshape(B, S, Hkv, D), layer["k_ctx"], layer["v_ctx"], ctx_len)
     o = bf16_round(o)                                                   # [Q3]
@@ -287,7 +327,8 @@ def layer_forward(h, layer, phi, dims, ctx_len=None):
 
 
 def denoise_step(dims, layers, phi_t, w_lm, tokens, masked, gamma, t, T,
-                 h=None, emb=None, pos=None, ctx_len=None, rule: int = RULE_CONFIDENCE):
+                 h=None, emb=None, pos=None, ctx_len=None, rule: int = RULE_CONFIDENCE,
+                 rope_theta: float = 0.0):
     """One denoising step: embed (if h is None), every layer, LM head, commit.
 
     Returns a dict with conf, pred, gap, tokens, masked, n_committed, committed, h_final.
@@ -298,7 +339,7 @@ def denoise_step(dims, layers, phi_t, w_lm, tokens, masked, gamma, t, T,
     else:
         h = as_f64(h)
     for layer in layers:
-        h, _ = layer_forward(h, layer, phi_t, dims, ctx_len)
+        h, _ = layer_forward(h, layer, phi_t, dims, ctx_len, rope_theta)
     conf, pred, gap, zmax = lmhead_confidence(h, w_lm)
     conf = conf.reshape(B, S); pred = pred.reshape(B, S); gap = gap.reshape(B, S)
     tok2, msk2, ncom, committed = commit(conf, pred, tokens, masked, gamma, force_all=(t == T),
@@ -309,7 +350,7 @@ def denoise_step(dims, layers, phi_t, w_lm, tokens, masked, gamma, t, T,
 
 def decode_block(dims, layers, phi_table, w_lm, emb, pos, gamma, T, tokens=None, masked=None,
                  t_start: int = 1, ctx_len=None, trace: bool = False,
-                 rule: int = RULE_CONFIDENCE):
+                 rule: int = RULE_CONFIDENCE, rope_theta: float = 0.0):
     """Block decode loop: starting from all [MASK] (or a given state), run steps
     t = t_start..T, stop after the first step that leaves nothing masked.
 
@@ -327,7 +368,7 @@ def decode_block(dims, layers, phi_table, w_lm, emb, pos, gamma, T, tokens=None,
         if not masked.any():
             break
         r = denoise_step(dims, layers, phi_table[t - 1], w_lm, tokens, masked, gamma, t, T,
-                         emb=emb, pos=pos, ctx_len=ctx_len, rule=rule)
+                         emb=emb, pos=pos, ctx_len=ctx_len, rule=rule, rope_theta=rope_theta)
         tokens, masked = r["tokens"], r["masked"]
         steps += 1
         if trace:

@@ -488,3 +488,35 @@ def test_kv_append_overflow_leaves_the_sequence_unchanged():
     assert list(ovf) == [True, False] and list(ln) == [7, 10]
     assert np.array_equal(k2[0], kc[0]) and np.array_equal(v2[0], vc[0])
     assert np.array_equal(k2[1, 0, 6:10], kn[1, :, 0])
+
+
+# ----------------------------------------------------------------------------- rotary variant
+
+def test_rope_is_a_rotation_and_identity_at_position_zero():
+    x = rng.standard_normal((5, 3, 64))
+    pos = np.array([0, 1, 7, 1000, 32767])
+    y = oracle.rope_rotate(x, pos, 10000.0)
+    assert np.array_equal(y[0], x[0])                                  # angle 0
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-13)
+    # pair 0 turns by exactly pos radians (theta**0 = 1): closed form for one pair
+    a = float(pos[2])
+    assert np.allclose(y[2, :, 0], x[2, :, 0] * math.cos(a) - x[2, :, 1] * math.sin(a))
+    assert np.allclose(y[2, :, 1], x[2, :, 0] * math.sin(a) + x[2, :, 1] * math.cos(a))
+    # the last pair's frequency is theta**(-(D-2)/D)
+    f = 10000.0 ** (-(64 - 2) / 64)
+    assert np.allclose(y[3, :, 62], x[3, :, 62] * math.cos(1000 * f) - x[3, :, 63] * math.sin(1000 * f))
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    # q . k after rotating both depends on p_q - p_k only (computed here with einsum)
+    q = rng.standard_normal((1, 1, 32)); k = rng.standard_normal((1, 1, 32))
+    s1 = np.einsum("rhd,rhd->", oracle.rope_rotate(q, [100], 500.0), oracle.rope_rotate(k, [90], 500.0))
+    s2 = np.einsum("rhd,rhd->", oracle.rope_rotate(q, [13], 500.0), oracle.rope_rotate(k, [3], 500.0))
+    s3 = np.einsum("rhd,rhd->", oracle.rope_rotate(q, [13], 500.0), oracle.rope_rotate(k, [4], 500.0))
+    assert abs(s1 - s2) < 1e-12 and abs(s1 - s3) > 1e-6
+
+
+def test_block_positions_follow_the_context():
+    dims = dict(B=2, S=3, Lmax=50)
+    assert list(oracle.block_positions(dims, [7, 0])) == [7, 8, 9, 0, 1, 2]
+    assert list(oracle.block_positions(dims)) == [50, 51, 52, 50, 51, 52]
