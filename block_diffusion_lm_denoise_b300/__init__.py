@@ -47,6 +47,10 @@ class td_layer(ctypes.Structure):
                 ("k_ctx", ctypes.c_void_p), ("v_ctx", ctypes.c_void_p)]
 
 
+class td_step_opts(ctypes.Structure):
+    _fields_ = [("rule", ctypes.c_int), ("rope_theta", ctypes.c_float)]
+
+
 class td_kv(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p)]
 
@@ -73,11 +77,11 @@ def lib() -> ctypes.CDLL:
         L.td_lmhead_commit.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, i, vp, vp, vp, vp,
                                        vp, vp, vp, sz, vp]
         L.td_denoise_step.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer), vp, vp,
-                                      vp, vp, vp, vp, i, i, f, i, vp, vp, vp, vp, vp, vp, vp,
-                                      sz, vp]
+                                      vp, vp, vp, vp, i, i, f, ctypes.POINTER(td_step_opts), vp,
+                                      vp, vp, vp, vp, vp, vp, sz, vp]
         L.td_decode_block.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer), vp, vp,
-                                      vp, vp, vp, i, i, f, i, vp, vp, vp, vp, vp, vp,
-                                      ctypes.POINTER(i), vp, sz, vp]
+                                      vp, vp, vp, i, i, f, ctypes.POINTER(td_step_opts), vp, vp,
+                                      vp, vp, vp, vp, ctypes.POINTER(i), vp, sz, vp]
         L.td_kv_append.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer),
                                    ctypes.POINTER(td_kv), vp, vp]
         L.td_device_error.argtypes = [ctypes.POINTER(i)]
@@ -222,8 +226,9 @@ def _layers(layers: Sequence[Dict[str, torch.Tensor]]):
 def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tokens, masked,
                     h=None, emb=None, pos=None, ctx_len=None, conf=None, pred=None,
                     n_committed=None, all_done=None, ws=None, stream=None,
-                    rule: int = TD_COMMIT_CONFIDENCE):
+                    rule: int = TD_COMMIT_CONFIDENCE, rope_theta: float = 0.0):
     """One denoising step; tokens / masked updated in place.
+    rule: commit rule; rope_theta > 0: rotary variant (see td_step_opts in include/td.h).
     Returns (conf, pred, n_committed, all_done)."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     dev = w_lm.device
@@ -234,7 +239,8 @@ def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tok
     arr = _layers(layers)
     _check("td_denoise_step",
            lib().td_denoise_step(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(h), _ptr(emb),
-                                 _ptr(pos), _ptr(w_lm), _ptr(phi_t), t, T, gamma, int(rule),
+                                 _ptr(pos), _ptr(w_lm), _ptr(phi_t), t, T, gamma,
+                                 ctypes.byref(td_step_opts(int(rule), float(rope_theta))),
                                  _ptr(tokens),
                                  _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
                                  _ptr(all_done), _ptr(ws), ws.numel(), _stream(stream)))
@@ -244,7 +250,7 @@ def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tok
 def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: float, tokens,
                     masked, t_start: int = 1, ctx_len=None, conf=None, pred=None,
                     n_committed=None, all_done=None, ws=None, stream=None,
-                    rule: int = TD_COMMIT_CONFIDENCE) -> int:
+                    rule: int = TD_COMMIT_CONFIDENCE, rope_theta: float = 0.0) -> int:
     """Runs the block decode loop in place on tokens / masked; returns the steps taken."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     dev = w_lm.device
@@ -256,7 +262,8 @@ def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: floa
     arr = _layers(layers)
     _check("td_decode_block",
            lib().td_decode_block(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(emb), _ptr(pos),
-                                 _ptr(w_lm), _ptr(phi_table), t_start, T, gamma, int(rule),
+                                 _ptr(w_lm), _ptr(phi_table), t_start, T, gamma,
+                                 ctypes.byref(td_step_opts(int(rule), float(rope_theta))),
                                  _ptr(tokens),
                                  _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
                                  _ptr(all_done), ctypes.byref(steps), _ptr(ws), ws.numel(),

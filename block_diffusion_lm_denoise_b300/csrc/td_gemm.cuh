@@ -24,11 +24,15 @@ enum { EPI_QKV = 0, EPI_RESID = 1, EPI_LMHEAD = 2 };
 struct GemmParams {
   int M, N, K;
   int m_tiles, n_tiles, items;
-  // EPI_QKV: columns [0, nq) -> q, [nq, nq + nk) -> k, [nq + nk, nq + 2 nk) -> v
+  // EPI_QKV: columns [0, nq) -> q, [nq, nq + nk) -> k, [nq + nk, nq + 2 nk) -> v; with
+  // rope_cs set, q and k are rotated before rounding: row r, pair j of a head (columns 2j,
+  // 2j + 1) by rope_cs[r * head_dim / 2 + j] = (cos, sin)
   uint16_t* q;
   uint16_t* k;
   uint16_t* v;
   int nq, nk;
+  const float2* rope_cs;
+  int head_dim;
   // EPI_RESID; with row_pos set, row r's result goes to row row_pos[r] of h_out instead of
   // back into h, and rows with row_pos[r] < 0 are not written
   uint16_t* h;
@@ -215,6 +219,18 @@ __global__ void __launch_bounds__(256, 1)
           for (int j = 0; j < 32; ++j) s += ex2_approx((v[j] - run_max) * 1.4426950408889634f);
           run_sum += s;
         } else if constexpr (EPI == EPI_QKV) {
+          if (row_ok && col0 < p.N && p.rope_cs != nullptr && col0 < p.nq + p.nk) {
+            // the 32 columns of a chunk lie in one head (head_dim is 64 or 128)
+            const int hd0 = (col0 < p.nq ? col0 : col0 - p.nq) % p.head_dim;
+            const float2* cs = p.rope_cs + (size_t)row * (p.head_dim / 2) + hd0 / 2;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 c = __ldg(&cs[j]);
+              const float a = v[2 * j], b = v[2 * j + 1];
+              v[2 * j] = a * c.x - b * c.y;
+              v[2 * j + 1] = a * c.y + b * c.x;
+            }
+          }
           if (row_ok && col0 < p.N) {
             uint16_t* dst;
             if (col0 < p.nq)

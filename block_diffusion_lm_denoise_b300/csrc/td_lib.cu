@@ -392,6 +392,7 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
 // ------------------------------------------------------------------------------------------
 struct StepWs {
   uint16_t *h, *xmod, *q, *k, *v, *o;
+  float2* rope;     // [B*S][D/2] (cos, sin) of the rotary variant
   uint16_t* h_lm;   // last layer's output, rows masked at the step start only (compacted)
   int* row_pos;     // [B*S] compact index of each row, -1 if committed
   int* m_count;     // number of rows in h_lm
@@ -415,6 +416,7 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
   const size_t o_q = take(M * dm->Hq * dm->D * 2), o_k = take(M * dm->Hkv * dm->D * 2),
                o_v = take(M * dm->Hkv * dm->D * 2), o_o = take(M * dm->Hq * dm->D * 2);
   const size_t o_hl = take(M * dm->d * 2), o_rp = take(M * 4), o_mc = take(16);
+  const size_t o_ro = take(M * (size_t)(dm->D / 2) * sizeof(float2));
   const size_t o_g = take((size_t)dm->d * 4);
   const size_t o_a = take(attn_ws_bytes(dm, nsm));
   const size_t o_l = take(lm_ws_bytes((int)M, dm->V));
@@ -429,6 +431,7 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
     w.v = reinterpret_cast<uint16_t*>(b + o_v);
     w.o = reinterpret_cast<uint16_t*>(b + o_o);
     w.h_lm = reinterpret_cast<uint16_t*>(b + o_hl);
+    w.rope = reinterpret_cast<float2*>(b + o_ro);
     w.row_pos = reinterpret_cast<int*>(b + o_rp);
     w.m_count = reinterpret_cast<int*>(b + o_mc);
     w.gate = reinterpret_cast<float*>(b + o_g);
@@ -441,8 +444,8 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
 
 td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len, const void* h,
                    const void* emb, const void* pos, const void* w_lm, const float* phi_t,
-                   int t, int T, float gamma, int rule, int* tokens, unsigned char* masked,
-                   float* conf,
+                   int t, int T, float gamma, int rule, float rope_theta, int* tokens,
+                   unsigned char* masked, float* conf,
                    int* pred, int* n_committed, int* all_done, void* ws, cudaStream_t st,
                    int nsm, const int* skip = nullptr, int* steps = nullptr) {
   const StepWs w = carve_step(dm, ws, nsm);
@@ -464,12 +467,20 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
   TD_CUDA(cudaGetLastError());
   const int nq = dm->Hq * dm->D, nk = dm->Hkv * dm->D;
   const int bn = M >= 512 ? 256 : 128;
+  if (rope_theta > 0.f) {
+    const int total = M * (dm->D / 2);
+    rope_table_kernel<<<(total + 255) / 256, 256, 0, st>>>(ctx_len, dm->B, dm->S, dm->Lmax, dm->D,
+                                                          (double)rope_theta, w.rope, skip);
+    TD_CUDA(cudaGetLastError());
+  }
   for (int l = 0; l < dm->n_layers; ++l) {
     const td_layer& L = layers[l];
     td_status sa = launch_adaln(w.h, L.ada_E, phi_t, M, d, kLnEps, w.xmod, w.gate, st, skip);
     if (sa != TD_OK) return sa;
     GemmParams g1{};
     g1.q = w.q; g1.k = w.k; g1.v = w.v; g1.nq = nq; g1.nk = nk; g1.skip = skip;
+    g1.rope_cs = rope_theta > 0.f ? w.rope : nullptr;
+    g1.head_dim = dm->D;
     td_status s = gemm_dispatch<EPI_QKV>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn);
     if (s != TD_OK) return s;
     s = run_attention(dm, w.q, w.k, w.v, L.k_ctx, L.v_ctx, ctx_len, w.o, nullptr, w.attn, st,
@@ -560,7 +571,8 @@ cudaStream_t capture_stream() {
 td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx_len,
                        const void* emb, const void* pos, const void* w_lm,
                        const float* phi_table, int t_start, int T, float gamma, int rule,
-                       int* tokens, unsigned char* masked, float* conf, int* pred,
+                       float rope_theta, int* tokens, unsigned char* masked, float* conf,
+                       int* pred,
                        int* n_committed, int* all_done, void* ws, size_t ws_bytes,
                        cudaStream_t st, int nsm, int* steps_taken, int* done) {
   const StepWs w = carve_step(dm, ws, nsm);
@@ -575,6 +587,9 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
   std::memcpy(&gbits, &gamma, 4);
   key.v.push_back(gbits);
   key.v.push_back((uint64_t)rule);
+  uint32_t rbits;
+  std::memcpy(&rbits, &rope_theta, 4);
+  key.v.push_back(rbits);
   for (int l = 0; l < dm->n_layers; ++l) {
     u(layers[l].wqkv); u(layers[l].wo); u(layers[l].ada_E); u(layers[l].k_ctx); u(layers[l].v_ctx);
   }
@@ -600,8 +615,9 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
       s = TD_ERR_CUDA;
     for (int t = t_start; t <= T && s == TD_OK; ++t)
       s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
-                   phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, tokens, masked,
-                   conf, pred, n_committed, all_done, ws, cs, nsm, all_done, w.loop);
+                   phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, rope_theta,
+                   tokens, masked, conf, pred, n_committed, all_done, ws, cs, nsm, all_done,
+                   w.loop);
     cudaGraph_t g = nullptr;
     const cudaError_t ee = cudaStreamEndCapture(cs, &g);
     if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
@@ -640,6 +656,13 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
 
 bool rule_ok(int rule) {
   return rule == TD_COMMIT_CONFIDENCE || rule == TD_COMMIT_LEFT_TO_RIGHT;
+}
+
+// Options of a step (NULL: confidence masking, no rotation); false if they are invalid.
+bool read_opts(const td_step_opts* opts, int* rule, float* rope_theta) {
+  *rule = opts ? opts->rule : TD_COMMIT_CONFIDENCE;
+  *rope_theta = opts ? opts->rope_theta : 0.f;
+  return rule_ok(*rule) && std::isfinite(*rope_theta) && *rope_theta >= 0.f;
 }
 
 bool ws_ok(const void* ws, size_t have, size_t need) {
@@ -730,12 +753,15 @@ td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm,
 
 td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* h, const void* emb, const void* pos, const void* w_lm,
-                          const float* phi_t, int t, int T, float gamma, int rule, int* tokens,
-                          unsigned char* masked, float* conf, int* pred, int* n_committed,
-                          int* all_done, void* ws, size_t ws_bytes, void* stream) {
+                          const float* phi_t, int t, int T, float gamma,
+                          const td_step_opts* opts, int* tokens, unsigned char* masked,
+                          float* conf, int* pred, int* n_committed, int* all_done, void* ws,
+                          size_t ws_bytes, void* stream) {
   td_status s = check_dims(dims, true);
   if (s != TD_OK) return s;
-  if (!rule_ok(rule)) return TD_ERR_INVALID_ARG;
+  int rule = 0;
+  float rope_theta = 0.f;
+  if (!read_opts(opts, &rule, &rope_theta)) return TD_ERR_INVALID_ARG;
   if ((s = check_layers(dims, layers)) != TD_OK) return s;
   if (!w_lm || !phi_t || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
     return TD_ERR_INVALID_ARG;
@@ -743,20 +769,22 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
   if (t < 1 || T < 1 || t > T || std::isnan(gamma)) return TD_ERR_INVALID_ARG;
   const int nsm = sm_count();
   if (!ws_ok(ws, ws_bytes, carve_step(dims, nullptr, nsm).total)) return TD_ERR_WORKSPACE;
-  return run_step(dims, layers, ctx_len, h, emb, pos, w_lm, phi_t, t, T, gamma, rule, tokens,
-                  masked,
+  return run_step(dims, layers, ctx_len, h, emb, pos, w_lm, phi_t, t, T, gamma, rule,
+                  rope_theta, tokens, masked,
                   conf, pred, n_committed, all_done, ws, (cudaStream_t)stream, nsm);
 }
 
 td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* emb, const void* pos, const void* w_lm,
-                          const float* phi_table, int t_start, int T, float gamma, int rule,
-                          int* tokens, unsigned char* masked, float* conf, int* pred,
-                          int* n_committed, int* all_done, int* steps_taken, void* ws,
-                          size_t ws_bytes, void* stream) {
+                          const float* phi_table, int t_start, int T, float gamma,
+                          const td_step_opts* opts, int* tokens, unsigned char* masked,
+                          float* conf, int* pred, int* n_committed, int* all_done,
+                          int* steps_taken, void* ws, size_t ws_bytes, void* stream) {
   td_status s = check_dims(dims, true);
   if (s != TD_OK) return s;
-  if (!rule_ok(rule)) return TD_ERR_INVALID_ARG;
+  int rule = 0;
+  float rope_theta = 0.f;
+  if (!read_opts(opts, &rule, &rope_theta)) return TD_ERR_INVALID_ARG;
   if ((s = check_layers(dims, layers)) != TD_OK) return s;
   if (!emb || !pos || !w_lm || !phi_table || !tokens || !masked || !conf || !pred ||
       !n_committed || !all_done || !steps_taken)
@@ -778,7 +806,7 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   int done = 0;
   if (t_start <= T) {
     s = decode_graph(dims, layers, ctx_len, emb, pos, w_lm, phi_table, t_start, T, gamma, rule,
-                     tokens, masked, conf, pred, n_committed, all_done, ws, ws_bytes, st, nsm,
+                     rope_theta, tokens, masked, conf, pred, n_committed, all_done, ws, ws_bytes, st, nsm,
                      steps_taken, &done);
     if (s == TD_OK) return done ? TD_OK : TD_ERR_NOT_CONVERGED;
     if (s != TD_ERR_UNSUPPORTED) return s;
@@ -787,8 +815,8 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   *steps_taken = 0;
   for (int t = t_start; t <= T; ++t) {
     s = run_step(dims, layers, ctx_len, nullptr, emb, pos, w_lm,
-                 phi_table + (size_t)(t - 1) * 6 * dims->d, t, T, gamma, rule, tokens, masked,
-                 conf, pred, n_committed, all_done, ws, st, nsm);
+                 phi_table + (size_t)(t - 1) * 6 * dims->d, t, T, gamma, rule, rope_theta,
+                 tokens, masked, conf, pred, n_committed, all_done, ws, st, nsm);
     if (s != TD_OK) return s;
     TD_CUDA(cudaMemcpyAsync(&done, all_done, sizeof(int), cudaMemcpyDeviceToHost, st));
     TD_CUDA(cudaStreamSynchronize(st));

@@ -402,6 +402,27 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// Rotary table of a step: row r = b*S + i sits at position ctx_len[b] + i (Lmax without
+// ctx_len); pair j of a head turns by pos * theta^(-2j / head_dim). The angle and its cosine
+// and sine are taken in double precision, then stored as float.
+__global__ void rope_table_kernel(const int* __restrict__ ctx_len, int B, int S, int Lmax,
+                                  int head_dim, double theta, float2* __restrict__ cs,
+                                  const int* skip) {
+  if (skip != nullptr && *skip != 0) return;
+  const int half = head_dim / 2;
+  const int total = B * S * half;
+  for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < total; x += gridDim.x * blockDim.x) {
+    const int j = x % half;
+    const int r = x / half;
+    const int b = r / S, i = r % S;
+    const int L = ctx_len != nullptr ? ctx_len[b] : Lmax;
+    const double ang = (double)(L + i) * pow(theta, -2.0 * (double)j / (double)head_dim);
+    double sn, cn;
+    sincos(ang, &sn, &cn);
+    cs[x] = make_float2((float)cn, (float)sn);
+  }
+}
+
 // Context-cache append: row ctx_len[b] + i of KV head g of a layer's cache receives
 // token i of head g of the block's keys / values ([B, S, Hkv, D], token-major). One thread
 // per 16-byte chunk; sequences whose cache would pass Lmax are skipped (flagged by the

@@ -92,6 +92,21 @@ typedef enum td_commit_rule {
   TD_COMMIT_LEFT_TO_RIGHT = 1
 } td_commit_rule;
 
+/* Options of a denoise step (td_denoise_step, td_decode_block); NULL means
+ * { TD_COMMIT_CONFIDENCE, 0 }.
+ *   rule        a td_commit_rule.
+ *   rope_theta  0: no positional rotation (the pages describe none; the embedding path adds
+ *               the caller's position table instead). > 0: rotary variant, a reading of a
+ *               piece the pages leave open: the block's q and k are rotated at their absolute
+ *               positions ctx_len[b] + i (Lmax when ctx_len is NULL) before their bf16
+ *               rounding, interleaved pairs (2j, 2j+1) of each head turned by
+ *               pos * rope_theta^(-2j/D); the cached context keys are taken as already rotated
+ *               by the context tower. Negative or non-finite: TD_ERR_INVALID_ARG. */
+typedef struct td_step_opts {
+  int rule;
+  float rope_theta;
+} td_step_opts;
+
 /* Selector for td_workspace_size(). */
 enum {
   TD_FN_ADALN_MODULATE = 0,
@@ -168,7 +183,8 @@ td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm,
  *   m = E_l + phi_t; x_mod = adaLN(h) as in td_adaln_modulate (eps = 1e-6);
  *   [q | k | v] = bf16(x_mod . wqkv^T); o = td_block_attention(...);
  *   h = bf16(h + m[2] * (o . wo^T))            (m[2] is the gate)
- * and finally td_lmhead_commit with the given rule and force_all = (t == T), evaluated only
+ * (with opts->rope_theta > 0 the q and k of the block are rotated, see td_step_opts)
+ * and finally td_lmhead_commit with opts->rule and force_all = (t == T), evaluated only
  * on the rows that can commit: those masked when the step starts, and under
  * TD_COMMIT_LEFT_TO_RIGHT before step T only the lowest masked row of each sequence
  * (committed rows need no logits; the last layer writes just those rows, compacted, and the
@@ -178,9 +194,10 @@ td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm,
  *   ctx_len int32 [B] device or NULL.  Other outputs as in td_lmhead_commit. */
 td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* h, const void* emb, const void* pos, const void* w_lm,
-                          const float* phi_t, int t, int T, float gamma, int rule, int* tokens,
-                          unsigned char* masked, float* conf, int* pred, int* n_committed,
-                          int* all_done, void* ws, size_t ws_bytes, void* stream);
+                          const float* phi_t, int t, int T, float gamma,
+                          const td_step_opts* opts, int* tokens, unsigned char* masked,
+                          float* conf, int* pred, int* n_committed, int* all_done, void* ws,
+                          size_t ws_bytes, void* stream);
 
 /* Block decode loop ([chathome] generation paragraph: a block starts as S [MASK] tokens,
  * is refined for T steps and committed). Runs td_denoise_step (embedding path) for
@@ -197,10 +214,10 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
  * happen with force-commit at t == T; kept for callers that stop early). */
 td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* emb, const void* pos, const void* w_lm,
-                          const float* phi_table, int t_start, int T, float gamma, int rule,
-                          int* tokens, unsigned char* masked, float* conf, int* pred,
-                          int* n_committed, int* all_done, int* steps_taken, void* ws,
-                          size_t ws_bytes, void* stream);
+                          const float* phi_table, int t_start, int T, float gamma,
+                          const td_step_opts* opts, int* tokens, unsigned char* masked,
+                          float* conf, int* pred, int* n_committed, int* all_done,
+                          int* steps_taken, void* ws, size_t ws_bytes, void* stream);
 
 /* The committed block's keys / values of one context-tower layer (the context tower's
  * forward pass itself is outside this library; its output is the input here).

@@ -64,7 +64,7 @@ def test_null_pointers_are_rejected_before_any_launch(lib):
     assert lib.td_adaln_modulate(None, None, None, 4, 256, 1e-6, None, None) == 1
     steps = ctypes.c_int(0)
     assert lib.td_decode_block(ctypes.byref(dm), None, None, None, None, None, None, 1, 16,
-                               0.8, 0, None, None, None, None, None, None, ctypes.byref(steps),
+                               0.8, None, None, None, None, None, None, None, ctypes.byref(steps),
                                None, 0, None) == 1
     assert lib.td_kv_append(ctypes.byref(dm), None, None, None, None) == 1
     # shapes outside the kernels' limits
@@ -87,3 +87,17 @@ def test_unknown_commit_rule_is_rejected(lib):
     fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the rule check fails first
     assert lib.td_lmhead_commit(ctypes.byref(dm), fake, fake, 0.8, 7, 0, fake, fake, fake, fake,
                                 fake, fake, fake, 1 << 30, None) == 1
+
+
+def test_invalid_step_options_are_rejected(lib):
+    dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=0)
+    fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the option check fails first
+    steps = ctypes.c_int(0)
+    for opts in (td.td_step_opts(5, 0.0), td.td_step_opts(0, -1.0),
+                 td.td_step_opts(0, float("nan"))):
+        assert lib.td_denoise_step(ctypes.byref(dm), None, None, fake, fake, fake, fake, fake, 1,
+                                   16, 0.8, ctypes.byref(opts), fake, fake, fake, fake, fake,
+                                   fake, fake, 1 << 30, None) == 1
+        assert lib.td_decode_block(ctypes.byref(dm), None, None, fake, fake, fake, fake, 1, 16,
+                                   0.8, ctypes.byref(opts), fake, fake, fake, fake, fake, fake,
+                                   ctypes.byref(steps), fake, 1 << 30, None) == 1

@@ -192,3 +192,48 @@ def test_three_blocks_with_the_cache_growing_between_them(cuda_device):
             cpu_layers[l]["v_ctx"] = torch.from_numpy(v2).to(torch.bfloat16)
         ctx_ref = [c + dm.S for c in ctx_ref]
         assert ctx.cpu().tolist() == ctx_ref
+
+
+@pytest.mark.parametrize("Hq,D", [(8, 64), (32, 128)])
+def test_denoise_step_rotary_variant_matches_oracle(cuda_device, Hq, D):
+    # Hq = 32, D = 128 runs the SM-pair attention, Hq = 8, D = 64 the single-SM one
+    theta = 10000.0
+    dm = synth.Dims(B=3, S=16, d=256, Hq=Hq, Hkv=2, D=D, V=1024, Lmax=150, n_layers=2)
+    layers, w_lm, emb, pos, phi = _small_model(71, dm, cuda_device)
+    masked = synth.bernoulli((dm.B, dm.S), 0.7, 71, "m", cuda_device).to(torch.uint8)
+    tokens = torch.where(masked.bool(), torch.full((dm.B, dm.S), dm.V, dtype=torch.int32,
+                                                   device=cuda_device),
+                         synth.integers((dm.B, dm.S), dm.V, 71, "tok", cuda_device))
+    ctx = torch.tensor([150, 61, 0], dtype=torch.int32, device=cuda_device)
+    t0, m0 = tokens.clone(), masked.clone()
+    conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[2], 3, 16, 0.8,
+                                                tokens, masked, emb=emb, pos=pos, ctx_len=ctx,
+                                                rope_theta=theta)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    cpu_layers = [{k: v.cpu() for k, v in L.items()} for L in layers]
+    m0n = m0.cpu().numpy().astype(bool)
+    r = oracle.denoise_step(dm.as_dict(), cpu_layers, phi[2].cpu(), w_lm.cpu(), t0.cpu().numpy(),
+                            m0n, 0.8, 3, 16, emb=emb.cpu(), pos=pos.cpu(), ctx_len=[150, 61, 0],
+                            rope_theta=theta)
+    ties = runner_up_ties(r["h_final"], w_lm.cpu(), pred.cpu().numpy(), r["pred"], r["gap"], m0n)
+    compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                           tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
+                   m0n, 0.8, step=True, tie_extra=ties, conf_band=STACKED_CONF_BAND)
+    # the rotation changes the result: the same step without it differs
+    r0 = oracle.denoise_step(dm.as_dict(), cpu_layers, phi[2].cpu(), w_lm.cpu(), t0.cpu().numpy(),
+                             m0n, 0.8, 3, 16, emb=emb.cpu(), pos=pos.cpu(), ctx_len=[150, 61, 0])
+    assert np.abs(r0["conf"] - r["conf"]).max() > 1e-4
+    # the loop entry point with the variant reproduces step-by-step calls bit for bit
+    tk = torch.full((dm.B, dm.S), dm.V, dtype=torch.int32, device=cuda_device)
+    mk = torch.ones((dm.B, dm.S), dtype=torch.uint8, device=cuda_device)
+    tb, mb = tk.clone(), mk.clone()
+    for t in range(1, dm.S + 1):
+        _, _, _, dn = td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[t - 1], t, dm.S, 0.8,
+                                         tk, mk, emb=emb, pos=pos, ctx_len=ctx, rope_theta=theta)
+        if int(dn.item()):
+            break
+    steps = td.td_decode_block(dm.as_dict(), layers, emb, pos, w_lm, phi, dm.S, 0.8, tb, mb,
+                               ctx_len=ctx, rope_theta=theta)
+    torch.cuda.synchronize()
+    assert steps == t and torch.equal(tb, tk) and not mb.any()
