@@ -47,8 +47,13 @@ class td_layer(ctypes.Structure):
                 ("k_ctx", ctypes.c_void_p), ("v_ctx", ctypes.c_void_p)]
 
 
+class td_paging(ctypes.Structure):
+    _fields_ = [("page_table", ctypes.c_void_p), ("max_pages", ctypes.c_int),
+                ("n_pages", ctypes.c_int)]
+
+
 class td_step_opts(ctypes.Structure):
-    _fields_ = [("rule", ctypes.c_int), ("rope_theta", ctypes.c_float)]
+    _fields_ = [("rule", ctypes.c_int), ("rope_theta", ctypes.c_float), ("paging", td_paging)]
 
 
 class td_kv(ctypes.Structure):
@@ -72,8 +77,8 @@ def lib() -> ctypes.CDLL:
         L.td_status_string.argtypes = [i]
         L.td_status_string.restype = ctypes.c_char_p
         L.td_adaln_modulate.argtypes = [vp, vp, vp, i, i, f, vp, vp]
-        L.td_block_attention.argtypes = [ctypes.POINTER(td_dims), vp, vp, vp, vp, vp, vp, vp, vp,
-                                         vp, sz, vp]
+        L.td_block_attention.argtypes = [ctypes.POINTER(td_dims), vp, vp, vp, vp, vp, vp,
+                                         ctypes.POINTER(td_paging), vp, vp, vp, sz, vp]
         L.td_lmhead_commit.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, i, vp, vp, vp, vp,
                                        vp, vp, vp, sz, vp]
         L.td_denoise_step.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer), vp, vp,
@@ -83,7 +88,7 @@ def lib() -> ctypes.CDLL:
                                       vp, vp, vp, i, i, f, ctypes.POINTER(td_step_opts), vp, vp,
                                       vp, vp, vp, vp, ctypes.POINTER(i), vp, sz, vp]
         L.td_kv_append.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer),
-                                   ctypes.POINTER(td_kv), vp, vp]
+                                   ctypes.POINTER(td_kv), vp, ctypes.POINTER(td_paging), vp]
         L.td_device_error.argtypes = [ctypes.POINTER(i)]
         L.td_lmhead_commit_static.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, vp, vp, vp,
                                                vp, vp, vp, vp]
@@ -156,8 +161,17 @@ def td_adaln_modulate(h: torch.Tensor, E: torch.Tensor, phi: torch.Tensor, eps: 
     return x_mod
 
 
+def _paging(page_table, n_pages):
+    """td_paging for a page table [B, max_pages] (int32 device tensor) or None."""
+    if page_table is None:
+        return None
+    return td_paging(_ptr(page_table), int(page_table.shape[1]), int(n_pages))
+
+
 def td_block_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len=None, o=None, lse=None,
-                       ws=None, stream=None):
+                       ws=None, stream=None, page_table=None, n_pages=0):
+    """page_table [B, max_pages] int32 with k_ctx / v_ctx as page pools [n_pages, Hkv, 128, D]
+    selects the paged layout."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     if o is None:
         o = torch.empty_like(q)
@@ -165,9 +179,19 @@ def td_block_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len=None, o=None
         ws = workspace(dm, TD_FN_BLOCK_ATTENTION, q.device)
     _check("td_block_attention",
            lib().td_block_attention(ctypes.byref(dm), _ptr(q), _ptr(k_blk), _ptr(v_blk),
-                                    _ptr(k_ctx), _ptr(v_ctx), _ptr(ctx_len), _ptr(o), _ptr(lse),
-                                    _ptr(ws), ws.numel(), _stream(stream)))
+                                    _ptr(k_ctx), _ptr(v_ctx), _ptr(ctx_len),
+                                    _byref_or_null(_paging(page_table, n_pages)), _ptr(o),
+                                    _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
     return o
+
+
+def _byref_or_null(x):
+    return None if x is None else ctypes.byref(x)
+
+
+def _opts(rule, rope_theta, page_table, n_pages):
+    pg = _paging(page_table, n_pages)
+    return td_step_opts(int(rule), float(rope_theta), pg if pg is not None else td_paging())
 
 
 def _outs(B, S, device, conf, pred, n_committed, all_done):
@@ -226,7 +250,8 @@ def _layers(layers: Sequence[Dict[str, torch.Tensor]]):
 def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tokens, masked,
                     h=None, emb=None, pos=None, ctx_len=None, conf=None, pred=None,
                     n_committed=None, all_done=None, ws=None, stream=None,
-                    rule: int = TD_COMMIT_CONFIDENCE, rope_theta: float = 0.0):
+                    rule: int = TD_COMMIT_CONFIDENCE, rope_theta: float = 0.0,
+                    page_table=None, n_pages: int = 0):
     """One denoising step; tokens / masked updated in place.
     rule: commit rule; rope_theta > 0: rotary variant (see td_step_opts in include/td.h).
     Returns (conf, pred, n_committed, all_done)."""
@@ -240,7 +265,7 @@ def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tok
     _check("td_denoise_step",
            lib().td_denoise_step(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(h), _ptr(emb),
                                  _ptr(pos), _ptr(w_lm), _ptr(phi_t), t, T, gamma,
-                                 ctypes.byref(td_step_opts(int(rule), float(rope_theta))),
+                                 ctypes.byref(_opts(rule, rope_theta, page_table, n_pages)),
                                  _ptr(tokens),
                                  _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
                                  _ptr(all_done), _ptr(ws), ws.numel(), _stream(stream)))
@@ -250,7 +275,8 @@ def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tok
 def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: float, tokens,
                     masked, t_start: int = 1, ctx_len=None, conf=None, pred=None,
                     n_committed=None, all_done=None, ws=None, stream=None,
-                    rule: int = TD_COMMIT_CONFIDENCE, rope_theta: float = 0.0) -> int:
+                    rule: int = TD_COMMIT_CONFIDENCE, rope_theta: float = 0.0,
+                    page_table=None, n_pages: int = 0) -> int:
     """Runs the block decode loop in place on tokens / masked; returns the steps taken."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     dev = w_lm.device
@@ -263,7 +289,7 @@ def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: floa
     _check("td_decode_block",
            lib().td_decode_block(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(emb), _ptr(pos),
                                  _ptr(w_lm), _ptr(phi_table), t_start, T, gamma,
-                                 ctypes.byref(td_step_opts(int(rule), float(rope_theta))),
+                                 ctypes.byref(_opts(rule, rope_theta, page_table, n_pages)),
                                  _ptr(tokens),
                                  _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
                                  _ptr(all_done), ctypes.byref(steps), _ptr(ws), ws.numel(),
@@ -271,7 +297,8 @@ def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: floa
     return steps.value
 
 
-def td_kv_append(dims, layers, block_kv, ctx_len, stream=None) -> None:
+def td_kv_append(dims, layers, block_kv, ctx_len, stream=None, page_table=None,
+                 n_pages: int = 0) -> None:
     """Appends each layer's committed-block keys / values (block_kv: a list of (k, v) device
     tensors [B, S, Hkv, D] bf16) to that layer's context cache at ctx_len, and grows
     ctx_len [B] (int32, device) by S, on the device."""
@@ -281,4 +308,5 @@ def td_kv_append(dims, layers, block_kv, ctx_len, stream=None) -> None:
     for i, (k, v) in enumerate(block_kv):
         kv[i] = td_kv(_ptr(k), _ptr(v))
     _check("td_kv_append", lib().td_kv_append(ctypes.byref(dm), arr, kv, _ptr(ctx_len),
+                                              _byref_or_null(_paging(page_table, n_pages)),
                                               _stream(stream)))

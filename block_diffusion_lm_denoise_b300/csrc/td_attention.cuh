@@ -52,6 +52,11 @@ struct AttnParams {
   float* lse;                // [B, S, Hq] or null
   float scale_log2;          // log2(e) / sqrt(D)
   const int* skip;           // when non-null and nonzero, return at once
+  // paged context cache: when page_table is set, each layer's cache is a pool
+  // [n_pages][Hkv][128][D] and logical 128-key tile t of sequence b is page
+  // page_table[b * max_pages + t]
+  const int* page_table;
+  int max_pages, n_pages;
 };
 
 constexpr int kKSlots = 3;         // K ring (a slot is freed when S of its tile is done)
@@ -79,6 +84,27 @@ __device__ __forceinline__ void pair_sync(int id) {
 
 __device__ __forceinline__ long long attn_lo(long long team, long long total, int n_teams) {
   return team * total / n_teams;
+}
+
+// TMA coordinates (key row, slab) of context tile t of (sequence b, KV head g): a contiguous
+// cache is one [Lmax][D] slab per (b, g); a paged cache is one [128][D] slab per (page, g).
+// An out-of-range page is flagged and read as zeros (slab -1 is outside the map).
+__device__ __forceinline__ bool attn_ctx_coords(const AttnParams& p, int b, int g, int t, int& y,
+                                                int& z) {
+  if (p.page_table == nullptr) {
+    y = t * kKeyTile;
+    z = b * p.Hkv + g;
+    return true;
+  }
+  const int page = p.page_table[(size_t)b * p.max_pages + t];
+  y = 0;
+  if (page < 0 || page >= p.n_pages) {
+    record_error(ERR_BAD_PAGE);
+    z = -1;
+    return false;
+  }
+  z = page * p.Hkv + g;
+  return true;
 }
 
 // One unit's share of a team's tile range.
@@ -257,17 +283,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int u = u_first; u <= u_last && ok; ++u) {
         const SegInfo s = attn_seg(p, lo, hi, u);
         if (attn_seg_work(p, s) == 0) continue;
-        const int row3 = s.b * p.Hkv + s.g;
         const int ctx_end = s.t1 < s.nvt ? s.t1 : s.nvt;     // live context tiles end here
         // L2 prefetch kPrefetch tiles ahead of the ring loads, so that a ring load mostly
         // hits L2 and its slot turns over in less time
-        for (int t = s.t0; t < s.t0 + kPrefetch && t < ctx_end; ++t)
-          for (int kh = 0; kh < D / 64; ++kh) tma_prefetch_l2_3d(mc, kh * 64, t * kKeyTile, row3);
+        auto prefetch = [&](int t) {
+          int y, z;
+          if (attn_ctx_coords(p, s.b, s.g, t, y, z))
+            for (int kh = 0; kh < D / 64; ++kh) tma_prefetch_l2_3d(mc, kh * 64, y, z);
+        };
+        for (int t = s.t0; t < s.t0 + kPrefetch && t < ctx_end; ++t) prefetch(t);
         for (int t = s.t0; t < s.t1; ++t) {
           if (!attn_tile_live(p, s, t)) continue;
-          if (t + kPrefetch < ctx_end)
-            for (int kh = 0; kh < D / 64; ++kh)
-              tma_prefetch_l2_3d(mc, kh * 64, (t + kPrefetch) * kKeyTile, row3);
+          if (t + kPrefetch < ctx_end) prefetch(t + kPrefetch);
           const int st = n % nslot;
           if (n >= nslot && !mbar_wait(&empty[st], ((n / nslot) & 1) ^ 1, ERR_WAIT_MMA)) {
             ok = false;
@@ -275,9 +302,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           uint8_t* dst = ring + st * L::kKBytes;
           if (t < p.n_ctx_tiles) {
+            int y, z;
+            attn_ctx_coords(p, s.b, s.g, t, y, z);
             mbar_arrive_expect_tx(&full[st], kKeyTile * 128 * (D / 64));
             for (int kh = 0; kh < D / 64; ++kh)
-              tma_load_3d(dst + kh * L::kKVHalf, mc, &full[st], kh * 64, t * kKeyTile, row3);
+              tma_load_3d(dst + kh * L::kKVHalf, mc, &full[st], kh * 64, y, z);
           } else {
             mbar_arrive_expect_tx(&full[st], p.S * 128 * (D / 64));
             for (int kh = 0; kh < D / 64; ++kh)

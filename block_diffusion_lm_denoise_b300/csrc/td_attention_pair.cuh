@@ -158,8 +158,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
       for (int u = u_first; u <= u_last && ok; ++u) {
         const SegInfo s = attn_seg(p, lo, hi, u);
         if (attn_seg_work(p, s) == 0) continue;
-        const int row3 = s.b * p.Hkv + s.g;
         const int ctx_end = s.t1 < s.nvt ? s.t1 : s.nvt;
+        // this CTA's half of context tile t: K rows 64r.. (both dim halves), V dims 64r..
+        auto prefetch = [&](int t) {
+          int y, z;
+          if (!attn_ctx_coords(p, s.b, s.g, t, y, z)) return;
+          if (is_v) tma_prefetch_l2_3d(mc, kx, y, z);
+          else
+            for (int kh = 0; kh < 2; ++kh) tma_prefetch_l2_3d(mc, kh * 64, y + ky, z);
+        };
         bool q_pending = !is_v;
         if (q_pending && sg == 0) {
           // the first Q goes out before the ring fills and prefetches queue up behind it
@@ -170,19 +177,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                              s.g * p.G + chunk * p.Gc, 0, s.b);
           ++sg;
         }
-        for (int t = s.t0; t < s.t0 + kPairPrefetch && t < ctx_end; ++t) {
-          if (is_v) tma_prefetch_l2_3d(mc, kx, t * kKeyTile, row3);
-          else
-            for (int kh = 0; kh < 2; ++kh) tma_prefetch_l2_3d(mc, kh * 64, t * kKeyTile + ky, row3);
-        }
+        for (int t = s.t0; t < s.t0 + kPairPrefetch && t < ctx_end; ++t) prefetch(t);
         for (int t = s.t0; t < s.t1; ++t) {
           if (!attn_tile_live(p, s, t)) continue;
-          if (t + kPairPrefetch < ctx_end) {
-            const int tp = (t + kPairPrefetch) * kKeyTile;
-            if (is_v) tma_prefetch_l2_3d(mc, kx, tp, row3);
-            else
-              for (int kh = 0; kh < 2; ++kh) tma_prefetch_l2_3d(mc, kh * 64, tp + ky, row3);
-          }
+          if (t + kPairPrefetch < ctx_end) prefetch(t + kPairPrefetch);
           const int st = n % nslot;
           if (n >= nslot && !mbar_wait(&empty[st], ((n / nslot) & 1) ^ 1, ERR_WAIT_MMA)) {
             ok = false;
@@ -192,10 +190,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
           if (even) mbar_arrive_expect_tx(&full[st], 2 * slot_bytes);   // both CTAs' halves
           uint8_t* dst = ring + st * slot_bytes;
           if (t < p.n_ctx_tiles) {
-            if (is_v) tma_load_3d_pair(dst, mc, bar, kx, t * kKeyTile, row3);
+            int y, z;
+            attn_ctx_coords(p, s.b, s.g, t, y, z);
+            if (is_v) tma_load_3d_pair(dst, mc, bar, kx, y, z);
             else
               for (int kh = 0; kh < 2; ++kh)
-                tma_load_3d_pair(dst + kh * L::kKHalf, mc, bar, kh * 64, t * kKeyTile + ky, row3);
+                tma_load_3d_pair(dst + kh * L::kKHalf, mc, bar, kh * 64, y + ky, z);
           } else {
             // the block keys: rows beyond S are out of bounds and arrive as zeros
             if (is_v) tma_load_4d_pair(dst, mb, bar, kx, s.g, 0, s.b);

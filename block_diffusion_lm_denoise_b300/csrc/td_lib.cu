@@ -311,9 +311,10 @@ td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, 
 }
 
 td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, const void* v_blk,
-                        const void* k_ctx, const void* v_ctx, const int* ctx_len, void* o,
-                        float* lse, void* ws, cudaStream_t st, int nsm,
-                        const int* skip = nullptr) {
+                        const void* k_ctx, const void* v_ctx, const int* ctx_len,
+                        const td_paging* pg, void* o, float* lse, void* ws, cudaStream_t st,
+                        int nsm, const int* skip = nullptr) {
+  const bool paged = pg != nullptr && pg->page_table != nullptr;
   const AttnPlan a = plan_attention(dm, nsm);
   const int D = dm->D;
   CUtensorMap mq, mkc, mvc, mkb, mvb;
@@ -339,11 +340,14 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
       return TD_ERR_CUDA;
   }
   {
-    // an empty cache still needs a well-formed (never used) descriptor
+    // an empty cache still needs a well-formed (never used) descriptor; a paged cache is one
+    // [128][D] slab per (page, KV head)
     const bool empty = dm->Lmax == 0;
-    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)(empty ? 1 : dm->Lmax),
-                              (uint64_t)(empty ? 1 : dm->B * dm->Hkv)};
-    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)(empty ? 1 : dm->Lmax) * D * 2};
+    const uint64_t rows = empty ? 1 : (paged ? (uint64_t)kKeyTile : (uint64_t)dm->Lmax);
+    const uint64_t slabs =
+        empty ? 1 : (paged ? (uint64_t)pg->n_pages * dm->Hkv : (uint64_t)dm->B * dm->Hkv);
+    const uint64_t dims[3] = {(uint64_t)D, rows, slabs};
+    const uint64_t str[2] = {(uint64_t)D * 2, rows * D * 2};
     const uint32_t boxk[3] = {64, kb_rows, 1};
     const uint32_t boxv[3] = {64, vb_rows, 1};
     const void* kb = empty ? k_blk : k_ctx;
@@ -360,6 +364,9 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
   p.ctx_len = ctx_len;
   p.q = static_cast<const uint16_t*>(q);
   p.skip = skip;
+  p.page_table = paged ? pg->page_table : nullptr;
+  p.max_pages = paged ? pg->max_pages : 0;
+  p.n_pages = paged ? pg->n_pages : 0;
   p.part_o = static_cast<float*>(ws);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + a.part_o_bytes);
   p.out = static_cast<uint16_t*>(o);
@@ -444,8 +451,8 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
 
 td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len, const void* h,
                    const void* emb, const void* pos, const void* w_lm, const float* phi_t,
-                   int t, int T, float gamma, int rule, float rope_theta, int* tokens,
-                   unsigned char* masked, float* conf,
+                   int t, int T, float gamma, int rule, float rope_theta,
+                   const td_paging* paging, int* tokens, unsigned char* masked, float* conf,
                    int* pred, int* n_committed, int* all_done, void* ws, cudaStream_t st,
                    int nsm, const int* skip = nullptr, int* steps = nullptr) {
   const StepWs w = carve_step(dm, ws, nsm);
@@ -483,8 +490,8 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
     g1.head_dim = dm->D;
     td_status s = gemm_dispatch<EPI_QKV>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn);
     if (s != TD_OK) return s;
-    s = run_attention(dm, w.q, w.k, w.v, L.k_ctx, L.v_ctx, ctx_len, w.o, nullptr, w.attn, st,
-                      nsm, skip);
+    s = run_attention(dm, w.q, w.k, w.v, L.k_ctx, L.v_ctx, ctx_len, paging, w.o, nullptr, w.attn,
+                      st, nsm, skip);
     if (s != TD_OK) return s;
     GemmParams g2{};
     g2.h = w.h; g2.gate = w.gate; g2.skip = skip;
@@ -571,8 +578,8 @@ cudaStream_t capture_stream() {
 td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx_len,
                        const void* emb, const void* pos, const void* w_lm,
                        const float* phi_table, int t_start, int T, float gamma, int rule,
-                       float rope_theta, int* tokens, unsigned char* masked, float* conf,
-                       int* pred,
+                       float rope_theta, const td_paging* paging, int* tokens,
+                       unsigned char* masked, float* conf, int* pred,
                        int* n_committed, int* all_done, void* ws, size_t ws_bytes,
                        cudaStream_t st, int nsm, int* steps_taken, int* done) {
   const StepWs w = carve_step(dm, ws, nsm);
@@ -590,6 +597,9 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
   uint32_t rbits;
   std::memcpy(&rbits, &rope_theta, 4);
   key.v.push_back(rbits);
+  u(paging ? paging->page_table : nullptr);
+  key.v.push_back(paging ? (uint64_t)paging->max_pages : 0);
+  key.v.push_back(paging ? (uint64_t)paging->n_pages : 0);
   for (int l = 0; l < dm->n_layers; ++l) {
     u(layers[l].wqkv); u(layers[l].wo); u(layers[l].ada_E); u(layers[l].k_ctx); u(layers[l].v_ctx);
   }
@@ -616,8 +626,8 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
     for (int t = t_start; t <= T && s == TD_OK; ++t)
       s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
                    phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, rope_theta,
-                   tokens, masked, conf, pred, n_committed, all_done, ws, cs, nsm, all_done,
-                   w.loop);
+                   paging, tokens, masked, conf, pred, n_committed, all_done, ws, cs, nsm,
+                   all_done, w.loop);
     cudaGraph_t g = nullptr;
     const cudaError_t ee = cudaStreamEndCapture(cs, &g);
     if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
@@ -658,11 +668,23 @@ bool rule_ok(int rule) {
   return rule == TD_COMMIT_CONFIDENCE || rule == TD_COMMIT_LEFT_TO_RIGHT;
 }
 
-// Options of a step (NULL: confidence masking, no rotation); false if they are invalid.
-bool read_opts(const td_step_opts* opts, int* rule, float* rope_theta) {
+// A paged layout must cover every sequence's Lmax and name a non-empty pool.
+bool paging_ok(const td_dims* dm, const td_paging* pg) {
+  if (pg == nullptr || pg->page_table == nullptr) return true;
+  const long long tiles = ((long long)dm->Lmax + kKeyTile - 1) / kKeyTile;
+  return pg->n_pages >= 1 && pg->max_pages >= tiles && pg->max_pages >= 1 &&
+         (long long)pg->n_pages * dm->Hkv < (1ll << 31);
+}
+
+// Options of a step (NULL: confidence masking, no rotation, contiguous caches); false if
+// they are invalid.
+bool read_opts(const td_dims* dm, const td_step_opts* opts, int* rule, float* rope_theta,
+               const td_paging** paging) {
   *rule = opts ? opts->rule : TD_COMMIT_CONFIDENCE;
   *rope_theta = opts ? opts->rope_theta : 0.f;
-  return rule_ok(*rule) && std::isfinite(*rope_theta) && *rope_theta >= 0.f;
+  *paging = (opts && opts->paging.page_table) ? &opts->paging : nullptr;
+  return rule_ok(*rule) && std::isfinite(*rope_theta) && *rope_theta >= 0.f &&
+         paging_ok(dm, *paging);
 }
 
 bool ws_ok(const void* ws, size_t have, size_t need) {
@@ -720,10 +742,11 @@ td_status td_adaln_modulate(const void* h, const float* E, const float* phi, int
 
 td_status td_block_attention(const td_dims* dims, const void* q, const void* k_blk,
                              const void* v_blk, const void* k_ctx, const void* v_ctx,
-                             const int* ctx_len, void* o, float* lse, void* ws, size_t ws_bytes,
-                             void* stream) {
+                             const int* ctx_len, const td_paging* paging, void* o, float* lse,
+                             void* ws, size_t ws_bytes, void* stream) {
   td_status s = check_dims(dims, false);
   if (s != TD_OK) return s;
+  if (!paging_ok(dims, paging)) return TD_ERR_INVALID_ARG;
   if (!q || !k_blk || !v_blk || !o) return TD_ERR_INVALID_ARG;
   if (dims->Lmax > 0 && (!k_ctx || !v_ctx)) return TD_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_blk) || !aligned16(v_blk) || !aligned16(o) ||
@@ -731,7 +754,7 @@ td_status td_block_attention(const td_dims* dims, const void* q, const void* k_b
     return TD_ERR_INVALID_ARG;
   const int nsm = sm_count();
   if (!ws_ok(ws, ws_bytes, attn_ws_bytes(dims, nsm))) return TD_ERR_WORKSPACE;
-  return run_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, o, lse, ws,
+  return run_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, paging, o, lse, ws,
                        (cudaStream_t)stream, nsm);
 }
 
@@ -761,7 +784,8 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
   if (s != TD_OK) return s;
   int rule = 0;
   float rope_theta = 0.f;
-  if (!read_opts(opts, &rule, &rope_theta)) return TD_ERR_INVALID_ARG;
+  const td_paging* paging = nullptr;
+  if (!read_opts(dims, opts, &rule, &rope_theta, &paging)) return TD_ERR_INVALID_ARG;
   if ((s = check_layers(dims, layers)) != TD_OK) return s;
   if (!w_lm || !phi_t || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
     return TD_ERR_INVALID_ARG;
@@ -770,7 +794,7 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
   const int nsm = sm_count();
   if (!ws_ok(ws, ws_bytes, carve_step(dims, nullptr, nsm).total)) return TD_ERR_WORKSPACE;
   return run_step(dims, layers, ctx_len, h, emb, pos, w_lm, phi_t, t, T, gamma, rule,
-                  rope_theta, tokens, masked,
+                  rope_theta, paging, tokens, masked,
                   conf, pred, n_committed, all_done, ws, (cudaStream_t)stream, nsm);
 }
 
@@ -784,7 +808,8 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   if (s != TD_OK) return s;
   int rule = 0;
   float rope_theta = 0.f;
-  if (!read_opts(opts, &rule, &rope_theta)) return TD_ERR_INVALID_ARG;
+  const td_paging* paging = nullptr;
+  if (!read_opts(dims, opts, &rule, &rope_theta, &paging)) return TD_ERR_INVALID_ARG;
   if ((s = check_layers(dims, layers)) != TD_OK) return s;
   if (!emb || !pos || !w_lm || !phi_table || !tokens || !masked || !conf || !pred ||
       !n_committed || !all_done || !steps_taken)
@@ -806,7 +831,7 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   int done = 0;
   if (t_start <= T) {
     s = decode_graph(dims, layers, ctx_len, emb, pos, w_lm, phi_table, t_start, T, gamma, rule,
-                     rope_theta, tokens, masked, conf, pred, n_committed, all_done, ws, ws_bytes, st, nsm,
+                     rope_theta, paging, tokens, masked, conf, pred, n_committed, all_done, ws, ws_bytes, st, nsm,
                      steps_taken, &done);
     if (s == TD_OK) return done ? TD_OK : TD_ERR_NOT_CONVERGED;
     if (s != TD_ERR_UNSUPPORTED) return s;
@@ -816,7 +841,7 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   for (int t = t_start; t <= T; ++t) {
     s = run_step(dims, layers, ctx_len, nullptr, emb, pos, w_lm,
                  phi_table + (size_t)(t - 1) * 6 * dims->d, t, T, gamma, rule, rope_theta,
-                 tokens, masked, conf, pred, n_committed, all_done, ws, st, nsm);
+                 paging, tokens, masked, conf, pred, n_committed, all_done, ws, st, nsm);
     if (s != TD_OK) return s;
     TD_CUDA(cudaMemcpyAsync(&done, all_done, sizeof(int), cudaMemcpyDeviceToHost, st));
     TD_CUDA(cudaStreamSynchronize(st));
@@ -827,9 +852,11 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
 }
 
 td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv* block_kv,
-                       int* ctx_len, void* stream) {
+                       int* ctx_len, const td_paging* paging, void* stream) {
   td_status s = check_dims(dims, false);
   if (s != TD_OK) return s;
+  if (!paging_ok(dims, paging)) return TD_ERR_INVALID_ARG;
+  const bool paged = paging != nullptr && paging->page_table != nullptr;
   if (dims->n_layers < 0 || (dims->n_layers > 0 && (!layers || !block_kv)) || !ctx_len)
     return TD_ERR_INVALID_ARG;
   if (dims->Lmax < dims->S) return TD_ERR_INVALID_ARG;   // a block can never fit
@@ -850,7 +877,8 @@ td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv*
         static_cast<const uint16_t*>(block_kv[l].k), static_cast<const uint16_t*>(block_kv[l].v),
         static_cast<uint16_t*>(const_cast<void*>(layers[l].k_ctx)),
         static_cast<uint16_t*>(const_cast<void*>(layers[l].v_ctx)), ctx_len, dims->B, dims->S,
-        dims->Hkv, dims->D, dims->Lmax);
+        dims->Hkv, dims->D, dims->Lmax, paged ? paging->page_table : nullptr,
+        paged ? paging->max_pages : 0, paged ? paging->n_pages : 0);
     TD_CUDA(cudaGetLastError());
   }
   kv_len_update_kernel<<<(dims->B + 255) / 256, 256, 0, st>>>(ctx_len, dims->B, dims->S,

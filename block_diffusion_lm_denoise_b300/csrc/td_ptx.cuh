@@ -21,7 +21,8 @@ enum : unsigned int {
   ERR_WAIT_EPI = 0x300,     // an epilogue / softmax hand-off did not complete in time
   ERR_TMEM = 0x400,         // TMEM allocation returned an unusable address
   ERR_BAD_TOKEN = 0x500,    // a token id outside [0, V] reached the embedding
-  ERR_CTX_FULL = 0x600      // a context-cache append would pass Lmax (or ctx_len < 0)
+  ERR_CTX_FULL = 0x600,     // a context-cache append would pass Lmax (or ctx_len < 0)
+  ERR_BAD_PAGE = 0x700      // a page-table entry outside [0, n_pages)
 };
 
 // ~2 s of polling (globaltimer ns) before a wait gives up.

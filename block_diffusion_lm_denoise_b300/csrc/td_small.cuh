@@ -427,10 +427,13 @@ __global__ void rope_table_kernel(const int* __restrict__ ctx_len, int B, int S,
 // token i of head g of the block's keys / values ([B, S, Hkv, D], token-major). One thread
 // per 16-byte chunk; sequences whose cache would pass Lmax are skipped (flagged by the
 // length update below).
+// With page_table set, the caches are pools [n_pages][Hkv][128][D] and position pos of
+// sequence b lives in page page_table[b * max_pages + pos / 128], row pos % 128.
 __global__ void kv_append_kernel(const uint16_t* __restrict__ k_new,
                                  const uint16_t* __restrict__ v_new, uint16_t* __restrict__ k_ctx,
                                  uint16_t* __restrict__ v_ctx, const int* __restrict__ ctx_len,
-                                 int B, int S, int Hkv, int D, int Lmax) {
+                                 int B, int S, int Hkv, int D, int Lmax,
+                                 const int* __restrict__ page_table, int max_pages, int n_pages) {
   const int c16 = D / 8;
   const long long total = (long long)B * S * Hkv * c16;
   for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < total;
@@ -442,7 +445,18 @@ __global__ void kv_append_kernel(const uint16_t* __restrict__ k_new,
     const int b = (int)(row / ((long long)Hkv * S));
     const int L = ctx_len[b];
     if (L < 0 || L + S > Lmax) continue;
-    const size_t dst = (((size_t)b * Hkv + g) * Lmax + (size_t)(L + i)) * D + (size_t)c * 8;
+    const int pos = L + i;
+    size_t dst;
+    if (page_table != nullptr) {
+      const int page = page_table[(size_t)b * max_pages + pos / 128];
+      if (page < 0 || page >= n_pages) {
+        record_error(ERR_BAD_PAGE);
+        continue;
+      }
+      dst = (((size_t)page * Hkv + g) * 128 + (size_t)(pos % 128)) * D + (size_t)c * 8;
+    } else {
+      dst = (((size_t)b * Hkv + g) * Lmax + (size_t)pos) * D + (size_t)c * 8;
+    }
     const size_t src = (size_t)row * D + (size_t)c * 8;
     *reinterpret_cast<uint4*>(k_ctx + dst) = *reinterpret_cast<const uint4*>(k_new + src);
     *reinterpret_cast<uint4*>(v_ctx + dst) = *reinterpret_cast<const uint4*>(v_new + src);

@@ -66,8 +66,9 @@ typedef struct td_dims {
  *   wo    bf16 [d, Hq*D]            W_o^T
  *   ada_E fp32 [6, d]               per-layer adaLN-single table E_l (rows: shift, scale,
  *                                   gate, then three rows of the out-of-scope MLP sublayer)
- *   k_ctx bf16 [B, Hkv, Lmax, D]    context keys of this layer (prompt + committed tokens)
- *   v_ctx bf16 [B, Hkv, Lmax, D]    context values of this layer */
+ *   k_ctx bf16 [B, Hkv, Lmax, D]    context keys of this layer (prompt + committed tokens),
+ *                                   or a page pool [n_pages, Hkv, 128, D] (td_paging)
+ *   v_ctx bf16 [B, Hkv, Lmax, D]    context values of this layer (same layout as k_ctx) */
 typedef struct td_layer {
   const void* wqkv;
   const void* wo;
@@ -92,8 +93,23 @@ typedef enum td_commit_rule {
   TD_COMMIT_LEFT_TO_RIGHT = 1
 } td_commit_rule;
 
+/* Paged context cache (optional; NULL or page_table == NULL: contiguous caches).
+ * With paging, every layer's k_ctx / v_ctx is a pool of 128-key pages, bf16
+ * [n_pages, Hkv, 128, D], and the keys of positions 128 t .. 128 t + 127 of sequence b (its
+ * logical context tile t) live in page page_table[b * max_pages + t]. Pages of a sequence need
+ * not be contiguous or ordered; sequences may share no page they write. Lmax still bounds every
+ * sequence's length (ctx_len[b] <= Lmax), and the entries for its tiles must be in
+ * [0, n_pages): an entry outside that range is read as zeros and flags ERR_BAD_PAGE (0x700) in
+ * the device error word.
+ *   page_table int32 [B, max_pages] device, max_pages >= ceil(Lmax / 128); n_pages >= 1. */
+typedef struct td_paging {
+  const int* page_table;
+  int max_pages;
+  int n_pages;
+} td_paging;
+
 /* Options of a denoise step (td_denoise_step, td_decode_block); NULL means
- * { TD_COMMIT_CONFIDENCE, 0 }.
+ * { TD_COMMIT_CONFIDENCE, 0, no paging }.
  *   rule        a td_commit_rule.
  *   rope_theta  0: no positional rotation (the pages describe none; the embedding path adds
  *               the caller's position table instead). > 0: rotary variant, a reading of a
@@ -101,10 +117,12 @@ typedef enum td_commit_rule {
  *               positions ctx_len[b] + i (Lmax when ctx_len is NULL) before their bf16
  *               rounding, interleaved pairs (2j, 2j+1) of each head turned by
  *               pos * rope_theta^(-2j/D); the cached context keys are taken as already rotated
- *               by the context tower. Negative or non-finite: TD_ERR_INVALID_ARG. */
+ *               by the context tower. Negative or non-finite: TD_ERR_INVALID_ARG.
+ *   paging      the context caches' layout (td_paging; page_table NULL: contiguous). */
 typedef struct td_step_opts {
   int rule;
   float rope_theta;
+  td_paging paging;
 } td_step_opts;
 
 /* Selector for td_workspace_size(). */
@@ -145,14 +163,16 @@ td_status td_adaln_modulate(const void* h, const float* E, const float* phi, int
  *   q      bf16 [B, S, Hq, D]       k_blk, v_blk bf16 [B, S, Hkv, D]
  *   k_ctx, v_ctx bf16 [B, Hkv, Lmax, D]
  *   ctx_len int32 [B] or NULL (0 <= ctx_len[b] <= Lmax)
+ *   paging  NULL (k_ctx, v_ctx contiguous as above) or a paged layout (td_paging: k_ctx,
+ *           v_ctx are page pools)
  *   o      bf16 [B, S, Hq, D] (written)
  *   lse    fp32 [B, S, Hq] or NULL: natural log of sum_j exp(q . keys_j / sqrt(D))
  *   ws     >= td_workspace_size(dims, TD_FN_BLOCK_ATTENTION) bytes.
  * Only B, S, Hq, Hkv, D, Lmax of dims are read. */
 td_status td_block_attention(const td_dims* dims, const void* q, const void* k_blk,
                              const void* v_blk, const void* k_ctx, const void* v_ctx,
-                             const int* ctx_len, void* o, float* lse, void* ws, size_t ws_bytes,
-                             void* stream);
+                             const int* ctx_len, const td_paging* paging, void* o, float* lse,
+                             void* ws, size_t ws_bytes, void* stream);
 
 /* LM head + confidence-masking commit ([chathome] generation and evaluation paragraphs:
  * tokens of the block commit when their confidence clears gamma; several commit per step).
@@ -236,10 +256,14 @@ typedef struct td_kv {
  *   ctx_len  int32 [B] device, in/out.
  * A sequence whose cache would pass Lmax (or whose ctx_len is negative) is left unchanged
  * and the device error word reads ERR_CTX_FULL (0x600, see td_device_error).
+ * With paging (non-NULL, page_table set) the caches are page pools and position pos of
+ * sequence b is written to row pos % 128 of page page_table[b * max_pages + pos / 128]; the
+ * caller maps the pages of the new positions before the call.
  * Only B, S, Hkv, D, Lmax, n_layers of dims are read. Errors: TD_ERR_INVALID_ARG (null or
- * misaligned pointers, Lmax < S). Asynchronous on stream; no workspace. */
+ * misaligned pointers, Lmax < S, a malformed td_paging). Asynchronous on stream; no
+ * workspace. */
 td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv* block_kv,
-                       int* ctx_len, void* stream);
+                       int* ctx_len, const td_paging* paging, void* stream);
 
 /* Reads and clears the device error word that bounded waits write (0 = none); the
  * current device is used. Synchronises the device. Returns TD_ERR_CUDA if the read fails. */

@@ -58,7 +58,7 @@ def test_null_pointers_are_rejected_before_any_launch(lib):
     dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=1)
     # every pointer null: validation must fail first
     assert lib.td_block_attention(ctypes.byref(dm), None, None, None, None, None, None, None,
-                                  None, None, 0, None) == 1
+                                  None, None, None, 0, None) == 1
     assert lib.td_lmhead_commit(ctypes.byref(dm), None, None, 0.8, 0, 0, None, None, None, None,
                                 None, None, None, 0, None) == 1
     assert lib.td_adaln_modulate(None, None, None, 4, 256, 1e-6, None, None) == 1
@@ -66,20 +66,20 @@ def test_null_pointers_are_rejected_before_any_launch(lib):
     assert lib.td_decode_block(ctypes.byref(dm), None, None, None, None, None, None, 1, 16,
                                0.8, None, None, None, None, None, None, None, ctypes.byref(steps),
                                None, 0, None) == 1
-    assert lib.td_kv_append(ctypes.byref(dm), None, None, None, None) == 1
+    assert lib.td_kv_append(ctypes.byref(dm), None, None, None, None, None) == 1
     # shapes outside the kernels' limits
     bad = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=80, V=1024, Lmax=64, n_layers=1)
     fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the shape check fails first
-    assert lib.td_block_attention(ctypes.byref(bad), fake, fake, fake, fake, fake, None, fake,
-                                  None, fake, 1 << 20, None) == 3
+    assert lib.td_block_attention(ctypes.byref(bad), fake, fake, fake, fake, fake, None, None,
+                                  fake, None, fake, 1 << 20, None) == 3
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake device pointers only without a GPU")
 def test_undersized_workspace_is_rejected(lib):
     dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=1)
     fake = ctypes.c_void_p(1 << 40)
-    assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None, fake,
-                                  None, fake, 16, None) == 2
+    assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None, None,
+                                  fake, None, fake, 16, None) == 2
 
 
 def test_unknown_commit_rule_is_rejected(lib):
@@ -101,3 +101,13 @@ def test_invalid_step_options_are_rejected(lib):
         assert lib.td_decode_block(ctypes.byref(dm), None, None, fake, fake, fake, fake, 1, 16,
                                    0.8, ctypes.byref(opts), fake, fake, fake, fake, fake, fake,
                                    ctypes.byref(steps), fake, 1 << 30, None) == 1
+
+
+def test_malformed_paging_is_rejected(lib):
+    dm = td.make_dims(B=2, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=300, n_layers=1)
+    fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the paging check fails first
+    for pg in (td.td_paging(fake, 2, 8),     # 2 columns cannot cover Lmax = 300 (3 tiles)
+               td.td_paging(fake, 3, 0)):    # empty pool
+        assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None,
+                                      ctypes.byref(pg), fake, None, fake, 1 << 30, None) == 1
+        assert lib.td_kv_append(ctypes.byref(dm), None, None, fake, ctypes.byref(pg), None) == 1

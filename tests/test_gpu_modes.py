@@ -11,7 +11,7 @@ import torch
 import block_diffusion_lm_denoise_b300 as td
 import oracle
 from block_diffusion_lm_denoise_b300 import synth
-from parity_util import STACKED_CONF_BAND, compare_commit, first_masked, runner_up_ties
+from parity_util import STACKED_CONF_BAND, attention_close, compare_commit, first_masked, runner_up_ties
 
 pytestmark = pytest.mark.gpu
 
@@ -237,3 +237,83 @@ def test_denoise_step_rotary_variant_matches_oracle(cuda_device, Hq, D):
                                ctx_len=ctx, rope_theta=theta)
     torch.cuda.synchronize()
     assert steps == t and torch.equal(tb, tk) and not mb.any()
+
+
+# ------------------------------------------------------------------------------ paged cache
+
+def _page_pool(cache, page_table, n_pages):
+    """A pool [n_pages, Hkv, 128, D] holding the contiguous cache [B, Hkv, Lmax, D] at the
+    pages page_table[b, t] (other pages and rows past Lmax: zeros)."""
+    B, Hkv, Lmax, D = cache.shape
+    pool = torch.zeros((n_pages, Hkv, 128, D), dtype=cache.dtype, device=cache.device)
+    for b in range(B):
+        for t in range((Lmax + 127) // 128):
+            rows = min(128, Lmax - 128 * t)
+            pool[int(page_table[b, t]), :, :rows] = cache[b, :, 128 * t:128 * t + rows]
+    return pool
+
+
+def _shuffled_pages(B, max_pages, n_pages, seed, device):
+    perm = synth.integers((n_pages,), 1 << 30, seed, "perm", "cpu").argsort()[: B * max_pages]
+    return perm.reshape(B, max_pages).to(torch.int32).to(device)
+
+
+@pytest.mark.parametrize("Hq,D", [(32, 128), (8, 64)])
+def test_paged_attention_equals_contiguous_and_oracle(cuda_device, Hq, D):
+    B, S, Hkv, Lmax = 3, 16, 2, 400
+    ctx = [400, 130, 0]
+    q = synth.normal((B, S, Hq, D), 1.0, 81, "q", cuda_device)
+    kb = synth.normal((B, S, Hkv, D), 1.0, 81, "kb", cuda_device)
+    vb = synth.normal((B, S, Hkv, D), 1.0, 81, "vb", cuda_device)
+    kc = synth.normal((B, Hkv, Lmax, D), 1.0, 81, "kc", cuda_device)
+    vc = synth.normal((B, Hkv, Lmax, D), 1.0, 81, "vc", cuda_device)
+    max_pages, n_pages = 4, 17
+    pt = _shuffled_pages(B, max_pages, n_pages, 81, cuda_device)
+    kp, vp = _page_pool(kc, pt.cpu(), n_pages), _page_pool(vc, pt.cpu(), n_pages)
+    ctx_t = torch.tensor(ctx, dtype=torch.int32, device=cuda_device)
+    dims = td.make_dims(B=B, S=S, d=64, Hq=Hq, Hkv=Hkv, D=D, V=8, Lmax=Lmax, n_layers=1)
+    o_c = td.td_block_attention(dims, q, kb, vb, kc, vc, ctx_t)
+    o_p = td.td_block_attention(dims, q, kb, vb, kp, vp, ctx_t, page_table=pt, n_pages=n_pages)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    assert torch.equal(o_c, o_p)
+    o_ref, _ = oracle.block_attention(q, kb, vb, kc, vc, ctx)
+    ok, worst = attention_close(_np(o_p), o_ref)
+    assert ok, worst
+
+
+def test_paged_append_and_step_equal_the_contiguous_layout(cuda_device):
+    dm = synth.Dims(B=3, S=16, d=256, Hq=32, Hkv=2, D=128, V=1024, Lmax=300, n_layers=2)
+    layers, w_lm, emb, pos, phi = _small_model(91, dm, cuda_device)
+    max_pages, n_pages = 3, 11
+    pt = _shuffled_pages(dm.B, max_pages, n_pages, 91, cuda_device)
+    paged = [dict(L, k_ctx=_page_pool(L["k_ctx"], pt.cpu(), n_pages),
+                  v_ctx=_page_pool(L["v_ctx"], pt.cpu(), n_pages)) for L in layers]
+    start = [120, 250, 0]
+    ctx_c = torch.tensor(start, dtype=torch.int32, device=cuda_device)
+    ctx_p = ctx_c.clone()
+    new = [(synth.normal((dm.B, dm.S, dm.Hkv, dm.D), 1.0, 91, f"kn{l}", cuda_device),
+            synth.normal((dm.B, dm.S, dm.Hkv, dm.D), 1.0, 91, f"vn{l}", cuda_device))
+           for l in range(dm.n_layers)]
+    before = [(L["k_ctx"].cpu(), L["v_ctx"].cpu()) for L in layers]
+    td.td_kv_append(dm.as_dict(), layers, new, ctx_c)
+    td.td_kv_append(dm.as_dict(), paged, new, ctx_p, page_table=pt, n_pages=n_pages)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    assert torch.equal(ctx_c, ctx_p) and ctx_p.cpu().tolist() == [s + dm.S for s in start]
+    for l in range(dm.n_layers):
+        k2, v2, _, _ = oracle.kv_append(before[l][0], before[l][1], start, new[l][0], new[l][1])
+        ref_pool = _page_pool(torch.from_numpy(k2).to(torch.bfloat16), pt.cpu(), n_pages)
+        assert torch.equal(paged[l]["k_ctx"].cpu(), ref_pool)
+        assert torch.equal(layers[l]["k_ctx"].cpu(), torch.from_numpy(k2).to(torch.bfloat16))
+    # one denoise step on either layout gives the same bits
+    outs = []
+    for lays, kw in ((layers, {}), (paged, dict(page_table=pt, n_pages=n_pages))):
+        tk = torch.full((dm.B, dm.S), dm.V, dtype=torch.int32, device=cuda_device)
+        mk = torch.ones((dm.B, dm.S), dtype=torch.uint8, device=cuda_device)
+        conf, pred, _, _ = td.td_denoise_step(dm.as_dict(), lays, w_lm, phi[0], 1, 16, 0.8, tk,
+                                              mk, emb=emb, pos=pos, ctx_len=ctx_c, **kw)
+        outs.append((conf.clone(), pred.clone(), tk.clone(), mk.clone()))
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
