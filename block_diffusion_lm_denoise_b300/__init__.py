@@ -28,7 +28,7 @@ TD_COMMIT_LEFT_TO_RIGHT = 1   # mock-AR reading: one commit per step, lowest mas
 # Every symbol the header declares (checked by the tests).
 EXPORTED = ("td_workspace_size", "td_status_string", "td_adaln_modulate", "td_block_attention",
             "td_lmhead_commit", "td_denoise_step", "td_decode_block", "td_device_error",
-            "td_lmhead_commit_static", "td_kv_append")
+            "td_lmhead_commit_static", "td_kv_append", "td_check_bounded_wait")
 
 
 class TdError(RuntimeError):
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
         L.td_kv_append.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer),
                                    ctypes.POINTER(td_kv), vp, ctypes.POINTER(td_paging), vp]
         L.td_device_error.argtypes = [ctypes.POINTER(i)]
+        L.td_check_bounded_wait.argtypes = [ctypes.c_uint, vp]
         L.td_lmhead_commit_static.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, vp, vp, vp,
                                                vp, vp, vp, vp]
         for name in EXPORTED:
@@ -310,3 +311,9 @@ def td_kv_append(dims, layers, block_kv, ctx_len, stream=None, page_table=None,
     _check("td_kv_append", lib().td_kv_append(ctypes.byref(dm), arr, kv, _ptr(ctx_len),
                                               _byref_or_null(_paging(page_table, n_pages)),
                                               _stream(stream)))
+
+
+def td_check_bounded_wait(limit_us: int, stream=None) -> None:
+    """Launches the bounded-wait diagnostic (see include/td.h); read the result with
+    td_device_error()."""
+    _check("td_check_bounded_wait", lib().td_check_bounded_wait(int(limit_us), _stream(stream)))

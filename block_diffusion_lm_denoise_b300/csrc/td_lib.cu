@@ -887,6 +887,13 @@ td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv*
   return TD_OK;
 }
 
+td_status td_check_bounded_wait(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 2000000u) return TD_ERR_INVALID_ARG;
+  wait_check_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(1000ull * limit_us);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
+}
+
 td_status td_device_error(int* code) {
   if (!code) return TD_ERR_INVALID_ARG;
   TD_CUDA(cudaDeviceSynchronize());

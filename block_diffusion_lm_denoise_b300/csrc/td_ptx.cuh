@@ -87,15 +87,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 }
 
 // Wait until the phase with the given parity has completed. Bounded: gives up after
-// kWaitLimitNs (or at once if another wait already failed), records `code`, returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int code) {
+// limit_ns (or at once if another wait already failed), records `code`, returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int code,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (;;) {
     if (mbar_try_wait(a, parity)) return true;
     if (error_pending()) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       record_error(code);
       return false;
     }

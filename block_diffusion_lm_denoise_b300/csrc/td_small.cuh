@@ -423,6 +423,16 @@ __global__ void rope_table_kernel(const int* __restrict__ ctx_len, int B, int S,
   }
 }
 
+// One thread waits, through the same bounded wait every kernel uses, on a barrier that
+// nothing completes: the wait must give up after limit_ns and record ERR_WAIT_EPI.
+__global__ void wait_check_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_wait(&bar, 0, ERR_WAIT_EPI, limit_ns);
+}
+
 // Context-cache append: row ctx_len[b] + i of KV head g of a layer's cache receives
 // token i of head g of the block's keys / values ([B, S, Hkv, D], token-major). One thread
 // per 16-byte chunk; sequences whose cache would pass Lmax are skipped (flagged by the

@@ -266,8 +266,19 @@ td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv*
                        int* ctx_len, const td_paging* paging, void* stream);
 
 /* Reads and clears the device error word that bounded waits write (0 = none); the
- * current device is used. Synchronises the device. Returns TD_ERR_CUDA if the read fails. */
+ * current device is used. Synchronises the device. Returns TD_ERR_CUDA if the read fails.
+ * Codes: 0x100 a TMA transfer, 0x200 an MMA, 0x300 a hand-off between warps did not complete
+ * within the wait limit (about 2 s); 0x400 unusable TMEM; 0x500 a token id outside [0, V]
+ * reached the embedding (it was read as [MASK]); 0x600 a cache append would pass Lmax;
+ * 0x700 a page-table entry outside [0, n_pages). The first code recorded is kept. */
 td_status td_device_error(int* code);
+
+/* Diagnostic: launches one thread that waits, through the bounded wait all kernels use, on a
+ * barrier that nothing completes, with a limit of limit_us microseconds (1 .. 2000000). The
+ * wait gives up and records 0x300 in the device error word instead of hanging; a caller can
+ * check that with td_device_error() (which also clears it) on its own GPU. No paper passage:
+ * a property of this library. Asynchronous on stream. */
+td_status td_check_bounded_wait(unsigned int limit_us, void* stream);
 
 /* td_lmhead_commit without a caller-provided workspace. The pages have no counterpart: this
  * is a convenience of the library for callers that cannot allocate device memory, such as
