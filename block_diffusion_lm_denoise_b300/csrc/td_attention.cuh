@@ -89,9 +89,11 @@ __device__ __forceinline__ long long attn_lo(long long team, long long total, in
 // TMA coordinates (key row, slab) of context tile t of (sequence b, KV head g): a contiguous
 // cache is one [Lmax][D] slab per (b, g); a paged cache is one [128][D] slab per (page, g).
 // An out-of-range page is flagged and read as zeros (slab -1 is outside the map).
+// kPaged is a compile-time choice, so the contiguous kernels carry no paging code.
+template <bool kPaged>
 __device__ __forceinline__ bool attn_ctx_coords(const AttnParams& p, int b, int g, int t, int& y,
                                                 int& z) {
-  if (p.page_table == nullptr) {
+  if constexpr (!kPaged) {
     y = t * kKeyTile;
     z = b * p.Hkv + g;
     return true;
@@ -191,7 +193,7 @@ __device__ __forceinline__ void cursor_next(TileCursor& c, const AttnParams& p, 
   cursor_next_segment(c, p, lo, hi, u_last);
 }
 
-template <int D>
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fused_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmKc,
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // hits L2 and its slot turns over in less time
         auto prefetch = [&](int t) {
           int y, z;
-          if (attn_ctx_coords(p, s.b, s.g, t, y, z))
+          if (attn_ctx_coords<kPaged>(p, s.b, s.g, t, y, z))
             for (int kh = 0; kh < D / 64; ++kh) tma_prefetch_l2_3d(mc, kh * 64, y, z);
         };
         for (int t = s.t0; t < s.t0 + kPrefetch && t < ctx_end; ++t) prefetch(t);
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint8_t* dst = ring + st * L::kKBytes;
           if (t < p.n_ctx_tiles) {
             int y, z;
-            attn_ctx_coords(p, s.b, s.g, t, y, z);
+            attn_ctx_coords<kPaged>(p, s.b, s.g, t, y, z);
             mbar_arrive_expect_tx(&full[st], kKeyTile * 128 * (D / 64));
             for (int kh = 0; kh < D / 64; ++kh)
               tma_load_3d(dst + kh * L::kKVHalf, mc, &full[st], kh * 64, y, z);

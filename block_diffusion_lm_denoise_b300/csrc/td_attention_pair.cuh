@@ -56,6 +56,7 @@ struct PairSmem {
   static constexpr int kBytes = kOffBar + 512 + 1024;
 };
 
+template <bool kPaged>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmKc,
@@ -162,7 +163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
         // this CTA's half of context tile t: K rows 64r.. (both dim halves), V dims 64r..
         auto prefetch = [&](int t) {
           int y, z;
-          if (!attn_ctx_coords(p, s.b, s.g, t, y, z)) return;
+          if (!attn_ctx_coords<kPaged>(p, s.b, s.g, t, y, z)) return;
           if (is_v) tma_prefetch_l2_3d(mc, kx, y, z);
           else
             for (int kh = 0; kh < 2; ++kh) tma_prefetch_l2_3d(mc, kh * 64, y + ky, z);
@@ -191,7 +192,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
           uint8_t* dst = ring + st * slot_bytes;
           if (t < p.n_ctx_tiles) {
             int y, z;
-            attn_ctx_coords(p, s.b, s.g, t, y, z);
+            attn_ctx_coords<kPaged>(p, s.b, s.g, t, y, z);
             if (is_v) tma_load_3d_pair(dst, mc, bar, kx, y, z);
             else
               for (int kh = 0; kh < 2; ++kh)

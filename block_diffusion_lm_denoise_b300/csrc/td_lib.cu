@@ -373,17 +373,17 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
   p.lse = lse;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   if (a.pair) {
-    TD_CUDA(set_smem(attn_pair_kernel, PairSmem::kBytes));
-    attn_pair_kernel<<<a.ncta, kAttnThreads, PairSmem::kBytes, st>>>(mq, mkc, mvc, mkb, mvb,
-                                                                      p);
+    auto k = paged ? attn_pair_kernel<true> : attn_pair_kernel<false>;
+    TD_CUDA(set_smem(k, PairSmem::kBytes));
+    k<<<a.ncta, kAttnThreads, PairSmem::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
   } else if (D == 128) {
-    TD_CUDA(set_smem(attn_fused_kernel<128>, AttnSmem<128>::kBytes));
-    attn_fused_kernel<128><<<a.ncta, kAttnThreads, AttnSmem<128>::kBytes, st>>>(mq, mkc, mvc, mkb,
-                                                                               mvb, p);
+    auto k = paged ? attn_fused_kernel<128, true> : attn_fused_kernel<128, false>;
+    TD_CUDA(set_smem(k, AttnSmem<128>::kBytes));
+    k<<<a.ncta, kAttnThreads, AttnSmem<128>::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
   } else {
-    TD_CUDA(set_smem(attn_fused_kernel<64>, AttnSmem<64>::kBytes));
-    attn_fused_kernel<64><<<a.ncta, kAttnThreads, AttnSmem<64>::kBytes, st>>>(mq, mkc, mvc, mkb,
-                                                                             mvb, p);
+    auto k = paged ? attn_fused_kernel<64, true> : attn_fused_kernel<64, false>;
+    TD_CUDA(set_smem(k, AttnSmem<64>::kBytes));
+    k<<<a.ncta, kAttnThreads, AttnSmem<64>::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
   }
   TD_CUDA(cudaGetLastError());
   if (a.split) {
@@ -538,9 +538,12 @@ void set_all_smem() {
   set_smem(gemm_tn_kernel<256, 4, EPI_QKV>, GemmSmem<256, 4>::kBytes);
   set_smem(gemm_tn_kernel<256, 4, EPI_RESID>, GemmSmem<256, 4>::kBytes);
   set_smem(gemm_tn_kernel<256, 4, EPI_LMHEAD>, GemmSmem<256, 4>::kBytes);
-  set_smem(attn_fused_kernel<128>, AttnSmem<128>::kBytes);
-  set_smem(attn_fused_kernel<64>, AttnSmem<64>::kBytes);
-  set_smem(attn_pair_kernel, PairSmem::kBytes);
+  set_smem(attn_fused_kernel<128, false>, AttnSmem<128>::kBytes);
+  set_smem(attn_fused_kernel<64, false>, AttnSmem<64>::kBytes);
+  set_smem(attn_pair_kernel<false>, PairSmem::kBytes);
+  set_smem(attn_fused_kernel<128, true>, AttnSmem<128>::kBytes);
+  set_smem(attn_fused_kernel<64, true>, AttnSmem<64>::kBytes);
+  set_smem(attn_pair_kernel<true>, PairSmem::kBytes);
   set_smem(adaln_modulate_kernel<1>, 2 * 256 * 1 * 4);
   set_smem(adaln_modulate_kernel<2>, 2 * 256 * 2 * 4);
   set_smem(adaln_modulate_kernel<4>, 2 * 256 * 4 * 4);
