@@ -1,6 +1,7 @@
 // td_gemm.cuh -- persistent tcgen05 GEMM  C[M, N] = A[M, K] * B[N, K]^T  (bf16 in, fp32
 // accumulate in TMEM) with three fused epilogues:
 //   EPI_QKV    : bf16 store of the [q | k | v] projection into three row-major tensors
+//   EPI_QKV_ROPE: the same with q and k rotated first (rotary positional variant)
 //   EPI_RESID  : gated residual  h[r, n] = bf16(h[r, n] + gate[n] * C[r, n])  (in place, or
 //                for the last layer of a step only the rows the LM head needs, compacted)
 //   EPI_LMHEAD : per row and per 128/256-column vocabulary tile, (max, lowest argmax,
@@ -19,7 +20,7 @@
 
 namespace td {
 
-enum { EPI_QKV = 0, EPI_RESID = 1, EPI_LMHEAD = 2 };
+enum { EPI_QKV = 0, EPI_RESID = 1, EPI_LMHEAD = 2, EPI_QKV_ROPE = 3 };
 
 struct GemmParams {
   int M, N, K;
@@ -218,8 +219,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) s += ex2_approx((v[j] - run_max) * 1.4426950408889634f);
           run_sum += s;
-        } else if constexpr (EPI == EPI_QKV) {
-          if (row_ok && col0 < p.N && p.rope_cs != nullptr && col0 < p.nq + p.nk) {
+        } else if constexpr (EPI == EPI_QKV || EPI == EPI_QKV_ROPE) {
+          if (EPI == EPI_QKV_ROPE && row_ok && col0 < p.N && col0 < p.nq + p.nk) {
             // the 32 columns of a chunk lie in one head (head_dim is 64 or 128)
             const int hd0 = (col0 < p.nq ? col0 : col0 - p.nq) % p.head_dim;
             const float2* cs = p.rope_cs + (size_t)row * (p.head_dim / 2) + hd0 / 2;

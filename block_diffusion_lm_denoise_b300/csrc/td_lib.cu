@@ -486,9 +486,12 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
     if (sa != TD_OK) return sa;
     GemmParams g1{};
     g1.q = w.q; g1.k = w.k; g1.v = w.v; g1.nq = nq; g1.nk = nk; g1.skip = skip;
-    g1.rope_cs = rope_theta > 0.f ? w.rope : nullptr;
+    g1.rope_cs = w.rope;
     g1.head_dim = dm->D;
-    td_status s = gemm_dispatch<EPI_QKV>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn);
+    td_status s =
+        rope_theta > 0.f
+            ? gemm_dispatch<EPI_QKV_ROPE>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn)
+            : gemm_dispatch<EPI_QKV>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn);
     if (s != TD_OK) return s;
     s = run_attention(dm, w.q, w.k, w.v, L.k_ctx, L.v_ctx, ctx_len, paging, w.o, nullptr, w.attn,
                       st, nsm, skip);
@@ -538,6 +541,8 @@ void set_all_smem() {
   set_smem(gemm_tn_kernel<256, 4, EPI_QKV>, GemmSmem<256, 4>::kBytes);
   set_smem(gemm_tn_kernel<256, 4, EPI_RESID>, GemmSmem<256, 4>::kBytes);
   set_smem(gemm_tn_kernel<256, 4, EPI_LMHEAD>, GemmSmem<256, 4>::kBytes);
+  set_smem(gemm_tn_kernel<128, 6, EPI_QKV_ROPE>, GemmSmem<128, 6>::kBytes);
+  set_smem(gemm_tn_kernel<256, 4, EPI_QKV_ROPE>, GemmSmem<256, 4>::kBytes);
   set_smem(attn_fused_kernel<128, false>, AttnSmem<128>::kBytes);
   set_smem(attn_fused_kernel<64, false>, AttnSmem<64>::kBytes);
   set_smem(attn_pair_kernel<false>, PairSmem::kBytes);
