@@ -289,19 +289,35 @@ __global__ void __launch_bounds__(1024)
     const float* pm = part_max + prow * n_tiles;
     const int* pa = part_arg + prow * n_tiles;
     const float* ps = part_sum + prow * n_tiles;
-    // lane-local pass over slices lane, lane+32, ...: max with the lowest slice on ties,
-    // and the exp-sum relative to a running max (rescaled when it grows)
+    // lane-local pass over slices lane, lane+32, ..., eight at a time (the loads of a batch
+    // are independent): max with the lowest slice on ties, and the exp-sum relative to a
+    // running max (rescaled when it grows)
     float m = -INFINITY, sum = 0.f;
     int mt = 0x7fffffff;
-    for (int t = lane; t < n_tiles; t += 32) {
-      const float v = __ldg(&pm[t]);
-      const float sv = __ldg(&ps[t]);
-      if (v > m) {
-        sum = (m == -INFINITY) ? 0.f : sum * ex2_approx((m - v) * 1.4426950408889634f);
-        m = v;
-        mt = t;
+    for (int t0 = lane; t0 < n_tiles; t0 += 32 * 8) {
+      float vm[8], vs[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int t = t0 + 32 * j;
+        vm[j] = t < n_tiles ? __ldg(&pm[t]) : -INFINITY;
+        vs[j] = t < n_tiles ? __ldg(&ps[t]) : 0.f;
       }
-      sum += sv * ex2_approx((v - m) * 1.4426950408889634f);
+      float cm = vm[0];
+      int ct = t0;
+#pragma unroll
+      for (int j = 1; j < 8; ++j)
+        if (vm[j] > cm) {
+          cm = vm[j];
+          ct = t0 + 32 * j;
+        }
+      if (cm > m) {
+        sum = (m == -INFINITY) ? 0.f : sum * ex2_approx((m - cm) * 1.4426950408889634f);
+        m = cm;
+        mt = ct;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (vm[j] != -INFINITY) sum += vs[j] * ex2_approx((vm[j] - m) * 1.4426950408889634f);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
