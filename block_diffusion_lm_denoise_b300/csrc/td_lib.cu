@@ -909,7 +909,10 @@ td_status td_device_error(int* code) {
   TD_CUDA(cudaMemcpyFromSymbol(&v, td::g_error_word, sizeof(v)));
   TD_CUDA(cudaMemcpyToSymbol(td::g_error_word, &zero, sizeof(zero)));
   *code = (int)v;
-  return TD_OK;
+  // a wait that ran out (TMA, MMA or hand-off) makes the call itself report it
+  return (v == td::ERR_WAIT_TMA || v == td::ERR_WAIT_MMA || v == td::ERR_WAIT_EPI)
+             ? TD_ERR_DEVICE_TIMEOUT
+             : TD_OK;
 }
 
 }  // extern "C"

@@ -29,7 +29,8 @@
  *   - Device-side waits are bounded. A kernel whose wait runs out records a code in a
  *     device error word and returns early; td_device_error() reads (and clears) it.
  *   - Shapes supported by the kernels: D in {64, 128}; Hq % Hkv == 0; 1 <= S <= 64;
- *     d % 64 == 0; V % 8 == 0; B*S <= 65536; Lmax >= 0.
+ *     d % 64 == 0 (and d <= 8192 for the denoise step); V % 8 == 0; B*S <= 65536;
+ *     Lmax >= 0.
  */
 #ifndef TD_H_
 #define TD_H_
@@ -48,7 +49,7 @@ typedef enum td_status {
   TD_ERR_UNSUPPORTED = 3,   /* a shape outside the limits listed above                  */
   TD_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch error, ...)           */
   TD_ERR_NOT_CONVERGED = 5, /* td_decode_block: positions still [MASK] after step T     */
-  TD_ERR_DEVICE_TIMEOUT = 6 /* a kernel's bounded wait ran out (see td_device_error)    */
+  TD_ERR_DEVICE_TIMEOUT = 6 /* td_device_error: a kernel's bounded wait ran out         */
 } td_status;
 
 /* Problem sizes (the pages' notation): B sequences, S block size, d hidden size,
@@ -266,7 +267,9 @@ td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv*
                        int* ctx_len, const td_paging* paging, void* stream);
 
 /* Reads and clears the device error word that bounded waits write (0 = none); the
- * current device is used. Synchronises the device. Returns TD_ERR_CUDA if the read fails.
+ * current device is used. Synchronises the device. Returns TD_ERR_DEVICE_TIMEOUT (with *code
+ * set) when the word holds a wait code (0x100, 0x200 or 0x300), TD_ERR_CUDA if the read fails,
+ * TD_OK otherwise.
  * Codes: 0x100 a TMA transfer, 0x200 an MMA, 0x300 a hand-off between warps did not complete
  * within the wait limit (about 2 s); 0x400 unusable TMEM; 0x500 a token id outside [0, V]
  * reached the embedding (it was read as [MASK]); 0x600 a cache append would pass Lmax;

@@ -1,6 +1,7 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out ends with an
 error code the host reads (and the context stays usable), and a corrupt input is flagged."""
 
+import ctypes
 import time
 
 import pytest
@@ -16,9 +17,10 @@ def test_a_wait_that_nothing_completes_gives_up_with_an_error_code(cuda_device):
     assert td.td_device_error() == 0
     t0 = time.perf_counter()
     td.td_check_bounded_wait(50000)          # 50 ms
-    code = td.td_device_error()              # synchronises
+    code = ctypes.c_int(0)
+    status = td.lib().td_device_error(ctypes.byref(code))   # synchronises
     el = time.perf_counter() - t0
-    assert code == 0x300
+    assert code.value == 0x300 and status == 6              # TD_ERR_DEVICE_TIMEOUT
     assert 0.045 <= el < 1.5, el
     # the context is still usable: a normal call runs and leaves no error
     B, S, Hq, Hkv, D, L = 1, 16, 4, 1, 64, 64
