@@ -317,3 +317,30 @@ def test_paged_append_and_step_equal_the_contiguous_layout(cuda_device):
     torch.cuda.synchronize()
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+def test_paged_attention_at_full_size_is_bit_identical_to_contiguous(cuda_device):
+    # the bench's attention shape: 64 sequences x 2 KV heads x 8192 keys, pages shuffled
+    wl = synth.attention_sweep(8192, cuda_device, B=64)
+    lay = wl.layers[0]
+    dm = wl.dims
+    B, Hkv, L, D = lay["k_ctx"].shape
+    T = L // 128
+    perm = synth.integers((B * T,), 1 << 30, 123, "perm", "cpu").argsort().to(cuda_device)
+    page_table = perm.reshape(B, T).to(torch.int32)
+
+    def pool_of(cache):
+        tiles = cache.view(B, Hkv, T, 128, D).permute(0, 2, 1, 3, 4).reshape(B * T, Hkv, 128, D)
+        pool = torch.empty_like(tiles)
+        pool[perm] = tiles
+        return pool
+
+    kp, vp = pool_of(lay["k_ctx"]), pool_of(lay["v_ctx"])
+    ctx = torch.tensor([L - 37 * b for b in range(B)], dtype=torch.int32, device=cuda_device)
+    o_c = td.td_block_attention(dm.as_dict(), lay["q"], lay["k_blk"], lay["v_blk"], lay["k_ctx"],
+                                lay["v_ctx"], ctx)
+    o_p = td.td_block_attention(dm.as_dict(), lay["q"], lay["k_blk"], lay["v_blk"], kp, vp, ctx,
+                                page_table=page_table, n_pages=B * T)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    assert torch.equal(o_c, o_p)
