@@ -225,8 +225,6 @@ td_status launch_gemm(const void* A, const void* Bm, int M, int N, int K, GemmPa
   gp.n_tiles = (N + BN - 1) / BN;
   gp.items = gp.m_tiles * gp.n_tiles;
   auto kern = gemm_tn_kernel<BN, STAGES, EPI>;
-  static bool attr_done[3] = {false, false, false};
-  (void)attr_done;
   TD_CUDA(set_smem(kern, L::kBytes));
   const int grid = std::min(gp.items, nsm);
   kern<<<grid, 256, L::kBytes, st>>>(ma, mb, gp);
