@@ -239,30 +239,17 @@ td_status gemm_dispatch(const void* A, const void* Bm, int M, int N, int K, Gemm
   return launch_gemm<256, 4, EPI>(A, Bm, M, N, K, gp, st, nsm);
 }
 
-template <int NK>
-td_status launch_adaln_nk(const void* h, const float* E, const float* phi, int rows, int d,
-                          float eps, void* x_mod, float* gate, cudaStream_t st, const int* skip) {
-  const int smem = 2 * d * (int)sizeof(float);
-  TD_CUDA(set_smem(adaln_modulate_kernel<NK>, smem));
-  adaln_modulate_kernel<NK><<<(rows + kAdaRows - 1) / kAdaRows, kAdaThreads, smem, st>>>(
-      static_cast<const uint16_t*>(h), E, phi, rows, d, eps, static_cast<uint16_t*>(x_mod), gate,
-      skip);
-  TD_CUDA(cudaGetLastError());
-  return TD_OK;
-}
-
-// adaLN-single modulation: the register path for d = 256 * NK (NK <= 32), else generic.
+// adaLN-single modulation: the column-slab path for d = 256 * k (d <= 8192) with 16-byte
+// aligned E and phi, else generic.
 td_status launch_adaln(const void* h, const float* E, const float* phi, int rows, int d,
                        float eps, void* x_mod, float* gate, cudaStream_t st,
                        const int* skip = nullptr) {
-  switch (d % 256 == 0 ? d / 256 : 0) {
-    case 1: return launch_adaln_nk<1>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
-    case 2: return launch_adaln_nk<2>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
-    case 4: return launch_adaln_nk<4>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
-    case 8: return launch_adaln_nk<8>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
-    case 16: return launch_adaln_nk<16>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
-    case 32: return launch_adaln_nk<32>(h, E, phi, rows, d, eps, x_mod, gate, st, skip);
-    default: break;
+  if (d % 256 == 0 && d / 8 <= 1024 && aligned16(E) && aligned16(phi)) {
+    adaln_slab_kernel<<<(rows + kAdaSlabRows - 1) / kAdaSlabRows, d / 8, 0, st>>>(
+        static_cast<const uint16_t*>(h), E, phi, rows, d, eps, static_cast<uint16_t*>(x_mod),
+        gate, skip);
+    TD_CUDA(cudaGetLastError());
+    return TD_OK;
   }
   adaln_modulate_generic_kernel<<<rows, 256, 0, st>>>(static_cast<const uint16_t*>(h), E, phi,
                                                       d, eps, static_cast<uint16_t*>(x_mod),
@@ -547,12 +534,6 @@ void set_all_smem() {
   set_smem(attn_fused_kernel<128, true>, AttnSmem<128>::kBytes);
   set_smem(attn_fused_kernel<64, true>, AttnSmem<64>::kBytes);
   set_smem(attn_pair_kernel<true>, PairSmem::kBytes);
-  set_smem(adaln_modulate_kernel<1>, 2 * 256 * 1 * 4);
-  set_smem(adaln_modulate_kernel<2>, 2 * 256 * 2 * 4);
-  set_smem(adaln_modulate_kernel<4>, 2 * 256 * 4 * 4);
-  set_smem(adaln_modulate_kernel<8>, 2 * 256 * 8 * 4);
-  set_smem(adaln_modulate_kernel<16>, 2 * 256 * 16 * 4);
-  set_smem(adaln_modulate_kernel<32>, 2 * 256 * 32 * 4);
 }
 
 struct LoopKey {

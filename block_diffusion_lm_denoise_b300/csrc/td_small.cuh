@@ -1,6 +1,6 @@
 // td_small.cuh -- the bandwidth-trivial steps of the denoise step:
 //   embed_kernel          h0[r] = bf16(emb[tokens[r]] + pos[r % S])
-//   adaln_modulate_kernel x_mod = bf16(LN(h) * (1 + scale) + shift), m = E + phi; also writes
+//   adaln_slab_kernel     x_mod = bf16(LN(h) * (1 + scale) + shift), m = E + phi; also writes
 //                         the gate row m[2] for the gated-residual epilogue
 //   merge_commit_kernel   merges the LM head's per-tile (max, argmax, exp-sum) partials into
 //                         conf / pred and applies the confidence-masking commit rule
@@ -38,111 +38,151 @@ __global__ void embed_kernel(const int* __restrict__ tokens, const uint16_t* __r
   }
 }
 
-// One warp per row, eight rows per CTA. The CTA first stages the modulation vectors
-// (1 + scale) and shift (m = E + phi, fp32) in shared memory; each lane then holds 8-element
-// slices c = 8 lane + 256 k of its row in registers (two-pass mean / variance, warp shuffles).
-constexpr int kAdaRows = 8;
-constexpr int kAdaThreads = 32 * kAdaRows;
 constexpr int kAdaMaxD = 8192;
 
-template <int NK>   // NK = d / 256 slices of 8 elements per lane
-__global__ void __launch_bounds__(kAdaThreads)
-    adaln_modulate_kernel(const uint16_t* __restrict__ h, const float* __restrict__ E,
-                          const float* __restrict__ phi, int rows, int d, float eps,
-                          uint16_t* __restrict__ x_mod, float* __restrict__ gate_out,
-                          const int* skip) {
-  if (skip != nullptr && *skip != 0) return;
-  constexpr int DD = 256 * NK;                 // d (the launcher checks d == 256 NK)
-  extern __shared__ float ada_sm[];            // [2][d]: 1 + scale, shift
-  float4* one_scale4 = reinterpret_cast<float4*>(ada_sm);
-  float4* shift4 = reinterpret_cast<float4*>(ada_sm + DD);
+// Column-slab layout: a CTA of d / 8 threads owns kAdaSlabRows rows; thread t owns columns
+// 8t .. 8t + 7 of every one of them and loads its eight-element slice of each row, all loads
+// in flight together. Row statistics in fp32: each thread takes the mean and the sum of
+// squared deviations of its own eight values (two passes over registers), and these pairs
+// are merged across the warp and then across the CTA with the pairwise update of Chan, Golub
+// and LeVeque ("Updating formulae and a pairwise algorithm for computing sample variances",
+// 1979): for parts of sizes na, nb with means ma, mb and squared-deviation sums Qa, Qb,
+// mean = ma + (mb - ma) nb / n and Q = Qa + Qb + (mb - ma)^2 na nb / n, n = na + nb. One
+// CTA-wide exchange instead of one for the mean and one for the variance. The modulation
+// values (1 + scale, shift) for the thread's columns are loaded while that exchange runs.
+constexpr int kAdaSlabRows = 4;
+
+__device__ __forceinline__ void chan_merge(float& n, float& m, float& q, float nb, float mb,
+                                           float qb) {
+  const float nn = n + nb;
+  if (nn > 0.f) {
+    const float dm = mb - m;
+    const float w = nb / nn;
+    m += dm * w;
+    q += qb + dm * dm * n * w;
+  }
+  n = nn;
+}
+
+__global__ void __launch_bounds__(1024)
+    adaln_slab_kernel(const uint16_t* __restrict__ h, const float* __restrict__ E,
+                      const float* __restrict__ phi, int rows, int d, float eps,
+                      uint16_t* __restrict__ x_mod, float* __restrict__ gate_out,
+                      const int* skip) {
+  constexpr int R = kAdaSlabRows;
+  __shared__ float2 red[R][32];         // [row][warp] (mean, squared-deviation sum)
+  __shared__ float2 stat[R];            // per row (mean, rstd)
+  const int t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int c0 = 8 * t;
+  const int r0 = blockIdx.x * R;
+  const bool skipped = skip != nullptr && *skip != 0;
+  uint4 raw[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+    raw[i] = (r0 + i < rows) ? *reinterpret_cast<const uint4*>(h + (size_t)(r0 + i) * d + c0)
+                             : make_uint4(0, 0, 0, 0);
+  if (skipped) return;
+  if (gate_out != nullptr && blockIdx.x == 0) {
+    const float4* e2 = reinterpret_cast<const float4*>(E + 2 * d + c0);
+    const float4* p2 = reinterpret_cast<const float4*>(phi + 2 * d + c0);
+    const float4 a0 = __ldg(&e2[0]), a1 = __ldg(&e2[1]), b0 = __ldg(&p2[0]), b1 = __ldg(&p2[1]);
+    float4* g = reinterpret_cast<float4*>(gate_out + c0);
+    g[0] = make_float4(a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w);
+    g[1] = make_float4(a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w);
+  }
+  auto unpack = [](const uint4& w, float (&x)[8]) {
+    x[0] = bf16lo_to_f32(w.x); x[1] = bf16hi_to_f32(w.x);
+    x[2] = bf16lo_to_f32(w.y); x[3] = bf16hi_to_f32(w.y);
+    x[4] = bf16lo_to_f32(w.z); x[5] = bf16hi_to_f32(w.z);
+    x[6] = bf16lo_to_f32(w.w); x[7] = bf16hi_to_f32(w.w);
+  };
+  // per-thread statistics of its eight values, then merged over the warp; the xor partners
+  // hold equal counts, so the merge reduces to mean = (ma + mb) / 2, Q = Qa + Qb + dm^2 n / 2
+  float mu[R], q[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    float x[8];
+    unpack(raw[i], x);
+    const float m = (((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]))) * 0.125f;
+    float qq = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float a = x[j] - m;
+      qq += a * a;
+    }
+    mu[i] = m;
+    q[i] = qq;
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float half_n = 4.0f * (float)o;   // n / 2 with n = 8 o values on each side
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const float mb = __shfl_xor_sync(0xffffffffu, mu[i], o);
+      const float qb = __shfl_xor_sync(0xffffffffu, q[i], o);
+      const float dm = mb - mu[i];
+      mu[i] = 0.5f * (mu[i] + mb);
+      q[i] = (q[i] + qb) + dm * dm * half_n;
+    }
+  }
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < R; ++i) red[i][warp] = make_float2(mu[i], q[i]);
+  // modulation slice: shift = E[0] + phi[0], 1 + scale = 1 + E[1] + phi[1]
+  float sh[8], sc[8];
   {
-    // fully unrolled float4 loads, all in flight at once
-    const float4* E4 = reinterpret_cast<const float4*>(E);
-    const float4* P4 = reinterpret_cast<const float4*>(phi);
-    constexpr int PER = DD / 4 / kAdaThreads;   // float4 per thread per vector (NK / 8 ... )
-    static_assert(DD % (4 * kAdaThreads) == 0 || NK < 4, "staging split");
-    if constexpr (DD >= 4 * kAdaThreads) {
-      float4 es[PER], ps[PER], eh[PER], ph[PER];
-#pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        const int i = threadIdx.x + j * kAdaThreads;
-        es[j] = __ldg(&E4[DD / 4 + i]); ps[j] = __ldg(&P4[DD / 4 + i]);
-        eh[j] = __ldg(&E4[i]); ph[j] = __ldg(&P4[i]);
-      }
-#pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        const int i = threadIdx.x + j * kAdaThreads;
-        one_scale4[i] = make_float4(1.0f + (es[j].x + ps[j].x), 1.0f + (es[j].y + ps[j].y),
-                                    1.0f + (es[j].z + ps[j].z), 1.0f + (es[j].w + ps[j].w));
-        shift4[i] = make_float4(eh[j].x + ph[j].x, eh[j].y + ph[j].y, eh[j].z + ph[j].z,
-                                eh[j].w + ph[j].w);
-      }
-    } else {
-      for (int i = threadIdx.x; i < DD / 4; i += kAdaThreads) {
-        const float4 es = __ldg(&E4[DD / 4 + i]), ps = __ldg(&P4[DD / 4 + i]);
-        const float4 eh = __ldg(&E4[i]), ph = __ldg(&P4[i]);
-        one_scale4[i] = make_float4(1.0f + (es.x + ps.x), 1.0f + (es.y + ps.y),
-                                    1.0f + (es.z + ps.z), 1.0f + (es.w + ps.w));
-        shift4[i] = make_float4(eh.x + ph.x, eh.y + ph.y, eh.z + ph.z, eh.w + ph.w);
-      }
-    }
+    const float4* e0 = reinterpret_cast<const float4*>(E + c0);
+    const float4* e1 = reinterpret_cast<const float4*>(E + d + c0);
+    const float4* p0 = reinterpret_cast<const float4*>(phi + c0);
+    const float4* p1 = reinterpret_cast<const float4*>(phi + d + c0);
+    const float4 a0 = __ldg(&e0[0]), a1 = __ldg(&e0[1]), b0 = __ldg(&p0[0]), b1 = __ldg(&p0[1]);
+    const float4 c0v = __ldg(&e1[0]), c1v = __ldg(&e1[1]), d0 = __ldg(&p1[0]), d1 = __ldg(&p1[1]);
+    sh[0] = a0.x + b0.x; sh[1] = a0.y + b0.y; sh[2] = a0.z + b0.z; sh[3] = a0.w + b0.w;
+    sh[4] = a1.x + b1.x; sh[5] = a1.y + b1.y; sh[6] = a1.z + b1.z; sh[7] = a1.w + b1.w;
+    sc[0] = 1.0f + (c0v.x + d0.x); sc[1] = 1.0f + (c0v.y + d0.y);
+    sc[2] = 1.0f + (c0v.z + d0.z); sc[3] = 1.0f + (c0v.w + d0.w);
+    sc[4] = 1.0f + (c1v.x + d1.x); sc[5] = 1.0f + (c1v.y + d1.y);
+    sc[6] = 1.0f + (c1v.z + d1.z); sc[7] = 1.0f + (c1v.w + d1.w);
   }
-  if (gate_out != nullptr && blockIdx.x == 0)
-    for (int c = threadIdx.x; c < DD; c += kAdaThreads) gate_out[c] = E[2 * DD + c] + phi[2 * DD + c];
-  const float* one_scale = ada_sm;
-  const float* shift = ada_sm + DD;
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * kAdaRows + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  const uint4* hr = reinterpret_cast<const uint4*>(h + (size_t)r * d);
-  uint4 raw[NK];
-#pragma unroll
-  for (int k = 0; k < NK; ++k) raw[k] = hr[lane + 32 * k];
-  float s = 0.f;
-#pragma unroll
-  for (int k = 0; k < NK; ++k) {
-    s += (bf16lo_to_f32(raw[k].x) + bf16hi_to_f32(raw[k].x)) +
-         (bf16lo_to_f32(raw[k].y) + bf16hi_to_f32(raw[k].y)) +
-         (bf16lo_to_f32(raw[k].z) + bf16hi_to_f32(raw[k].z)) +
-         (bf16lo_to_f32(raw[k].w) + bf16hi_to_f32(raw[k].w));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  const float mean = s / (float)d;
-  float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < NK; ++k) {
-    const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float a = bf16lo_to_f32(w[j]) - mean, b = bf16hi_to_f32(w[j]) - mean;
-      ss += a * a + b * b;
+  for (int i = warp; i < R; i += nwarps) {   // row i merged over the CTA's warps (256 values each)
+    float n = 0.f, m = 0.f, qq = 0.f;
+    if (lane < nwarps) {
+      const float2 v = red[i][lane];
+      n = 256.f;
+      m = v.x;
+      qq = v.y;
     }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float nb = __shfl_xor_sync(0xffffffffu, n, o);
+      const float mb = __shfl_xor_sync(0xffffffffu, m, o);
+      const float qb = __shfl_xor_sync(0xffffffffu, qq, o);
+      chan_merge(n, m, qq, nb, mb, qb);
+    }
+    if (lane == 0) stat[i] = make_float2(m, 1.0f / sqrtf(qq / (float)d + eps));
   }
+  __syncthreads();
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float rstd = 1.0f / sqrtf(ss / (float)d + eps);
-  uint4* out = reinterpret_cast<uint4*>(x_mod + (size_t)r * d);
-#pragma unroll
-  for (int k = 0; k < NK; ++k) {
-    const int c0 = 8 * (lane + 32 * k);
-    const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+  for (int i = 0; i < R; ++i) {
+    if (r0 + i >= rows) break;
+    const float2 st = stat[i];
+    float x[8];
+    unpack(raw[i], x);
     uint32_t o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = c0 + 2 * j;
-      const float y0 = (bf16lo_to_f32(w[j]) - mean) * rstd * one_scale[c] + shift[c];
-      const float y1 = (bf16hi_to_f32(w[j]) - mean) * rstd * one_scale[c + 1] + shift[c + 1];
-      o[j] = pack_bf16x2(y0, y1);
-    }
-    out[lane + 32 * k] = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int j = 0; j < 4; ++j)
+      o[j] = pack_bf16x2((x[2 * j] - st.x) * st.y * sc[2 * j] + sh[2 * j],
+                         (x[2 * j + 1] - st.x) * st.y * sc[2 * j + 1] + sh[2 * j + 1]);
+    *reinterpret_cast<uint4*>(x_mod + (size_t)(r0 + i) * d + c0) =
+        make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
-// Launch helper: d must be a multiple of 256 for the register path; other multiples of 8
-// take the generic one-CTA-per-row path below.
+// Any d that is a multiple of 8 (or E / phi off a 16-byte boundary): one CTA per row,
+// scalar loads.
 __global__ void __launch_bounds__(256)
     adaln_modulate_generic_kernel(const uint16_t* __restrict__ h, const float* __restrict__ E,
                                   const float* __restrict__ phi, int d, float eps,

@@ -29,11 +29,19 @@ def _no_device_error():
 
 # ------------------------------------------------------------------------------ adaLN
 
-@pytest.mark.parametrize("rows,d", [(16, 256), (37, 4096), (130, 1024)])
-def test_adaln_modulate_matches_oracle(cuda_device, rows, d):
+# (rows, d, misaligned): d = 256 k takes the column-slab kernel (8192: 1024 threads a CTA),
+# d = 264 and E / phi starting off a 16-byte boundary take the generic kernel
+@pytest.mark.parametrize("rows,d,misaligned", [(16, 256, False), (37, 4096, False),
+                                               (130, 1024, False), (5, 8192, False),
+                                               (3, 264, False), (9, 512, True)])
+def test_adaln_modulate_matches_oracle(cuda_device, rows, d, misaligned):
     h = synth.normal((rows, d), 1.7, 5, f"h{rows}", cuda_device)
     E = synth.normal((6, d), 0.02, 5, "E", cuda_device, torch.float32)
     phi = synth.normal((6, d), 0.25, 5, "phi", cuda_device, torch.float32)
+    if misaligned:
+        E = torch.cat([E.new_zeros(1), E.reshape(-1)])[1:].view(6, d)
+        phi = torch.cat([phi.new_zeros(1), phi.reshape(-1)])[1:].view(6, d)
+        assert E.data_ptr() % 16 != 0 and phi.data_ptr() % 16 != 0
     out = td.td_adaln_modulate(h, E, phi)
     torch.cuda.synchronize()
     _no_device_error()
