@@ -180,15 +180,55 @@ __global__ void __launch_bounds__(256, 1)
       const int mt = item % m_tiles;
       const int nt = item / m_tiles;
       const int acc = lt & 1;
-      if (!mbar_wait(&acc_full[acc], (lt >> 1) & 1, ERR_WAIT_MMA)) break;
-      tc_fence_after();
       const int row = mt * 128 + row_in_tile;
       const bool row_ok = row < M;
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      int out_row = row;
       if constexpr (EPI == EPI_RESID) {
-        if (p.row_pos != nullptr) out_row = row_ok ? p.row_pos[row] : -1;
+        // The residual slice of this thread's row is loaded while the MMAs run, so the
+        // epilogue waits on no global load once the accumulator is ready.
+        const int out_row = !row_ok ? -1 : (p.row_pos != nullptr ? p.row_pos[row] : row);
+        const bool live = out_row >= 0;
+        uint4 hreg[BN / 8];
+        const uint4* h4 = reinterpret_cast<const uint4*>(p.h + (size_t)row * p.N + nt * BN);
+#pragma unroll
+        for (int j = 0; j < BN / 8; ++j)
+          hreg[j] = (live && nt * BN + 8 * j < p.N) ? h4[j] : make_uint4(0, 0, 0, 0);
+        if (!mbar_wait(&acc_full[acc], (lt >> 1) & 1, ERR_WAIT_MMA)) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+        uint4* o4 = reinterpret_cast<uint4*>((p.row_pos != nullptr ? p.h_out : p.h) +
+                                             (size_t)out_row * p.N + nt * BN);
+        const float4* g4 = reinterpret_cast<const float4*>(p.gate + nt * BN);
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          tmem_ld_wait();
+          if (live && nt * BN + c * 32 < p.N) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 hv = hreg[4 * c + j];
+              const float4 ga = __ldg(&g4[8 * c + 2 * j]);
+              const float4 gb = __ldg(&g4[8 * c + 2 * j + 1]);
+              uint4 w;
+              w.x = pack_bf16x2(bf16lo_to_f32(hv.x) + ga.x * v[8 * j + 0],
+                                bf16hi_to_f32(hv.x) + ga.y * v[8 * j + 1]);
+              w.y = pack_bf16x2(bf16lo_to_f32(hv.y) + ga.z * v[8 * j + 2],
+                                bf16hi_to_f32(hv.y) + ga.w * v[8 * j + 3]);
+              w.z = pack_bf16x2(bf16lo_to_f32(hv.z) + gb.x * v[8 * j + 4],
+                                bf16hi_to_f32(hv.z) + gb.y * v[8 * j + 5]);
+              w.w = pack_bf16x2(bf16lo_to_f32(hv.w) + gb.z * v[8 * j + 6],
+                                bf16hi_to_f32(hv.w) + gb.w * v[8 * j + 7]);
+              o4[4 * c + j] = w;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
+        continue;
       }
+      if (!mbar_wait(&acc_full[acc], (lt >> 1) & 1, ERR_WAIT_MMA)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
 
       float run_max = -INFINITY, run_sum = 0.f;
       int run_arg = 0;
@@ -249,29 +289,6 @@ __global__ void __launch_bounds__(256, 1)
               w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
               w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
               d4[j] = w;
-            }
-          }
-        } else {  // EPI_RESID
-          if (row_ok && col0 < p.N && out_row >= 0) {
-            const uint4* h4 = reinterpret_cast<const uint4*>(p.h + (size_t)row * p.N + col0);
-            uint4* o4 = reinterpret_cast<uint4*>(
-                (p.row_pos != nullptr ? p.h_out : p.h) + (size_t)out_row * p.N + col0);
-            const float4* g4 = reinterpret_cast<const float4*>(p.gate + col0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 hv = h4[j];
-              const float4 ga = __ldg(&g4[2 * j]);
-              const float4 gb = __ldg(&g4[2 * j + 1]);
-              uint4 w;
-              w.x = pack_bf16x2(bf16lo_to_f32(hv.x) + ga.x * v[8 * j + 0],
-                                bf16hi_to_f32(hv.x) + ga.y * v[8 * j + 1]);
-              w.y = pack_bf16x2(bf16lo_to_f32(hv.y) + ga.z * v[8 * j + 2],
-                                bf16hi_to_f32(hv.y) + ga.w * v[8 * j + 3]);
-              w.z = pack_bf16x2(bf16lo_to_f32(hv.z) + gb.x * v[8 * j + 4],
-                                bf16hi_to_f32(hv.z) + gb.y * v[8 * j + 5]);
-              w.w = pack_bf16x2(bf16lo_to_f32(hv.w) + gb.z * v[8 * j + 6],
-                                bf16hi_to_f32(hv.w) + gb.w * v[8 * j + 7]);
-              o4[j] = w;
             }
           }
         }
