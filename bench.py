@@ -228,6 +228,9 @@ def main():
     ap.add_argument("--only", choices=["attention", "lmhead", "step"],
                     help="launch one kernel family alone, or one denoise step of one layer "
                          "(for profiler captures)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the attention over context lengths and the LM head over row "
+                         "counts, one JSON line per case (L2 flushed before every launch)")
     ap.add_argument("--B", type=int, default=32)
     ap.add_argument("--L", type=int, default=8192)
     ap.add_argument("--M", type=int, default=1024)
@@ -242,6 +245,9 @@ def main():
         return
     if args.only:
         run_only(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
 
     import block_diffusion_lm_denoise_b300 as td
@@ -471,6 +477,94 @@ def run_only(args):
     torch.cuda.synchronize()
     assert td.td_device_error() == 0
     print(json.dumps({"only": args.only, "reps": args.reps, "ok": True}))
+
+
+def run_sweep(args):
+    """Isolated kernel timings over the attention and LM-head workloads: attention with B = 32
+    sequences at context L in {512, 2048, 8192, 32768}; LM head + commit at M = B*S rows in
+    {16, 256, 1024, 4096} (S = 16, gamma 0.8, all rows masked). Before every timed launch a
+    512 MiB buffer is written and then another 256 MiB read, so no input is served from L2
+    and no write-back of the flush competes with the launch; each launch is timed with its
+    own pair of CUDA events on the launching stream, all launches queued behind a device-side
+    spin so that the host is ahead of the device."""
+    import block_diffusion_lm_denoise_b300 as td
+    from block_diffusion_lm_denoise_b300 import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk, pk_kind = peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.ones(256 << 20 >> 3, dtype=torch.int64, device=dev)
+    reps = max(args.reps, 10)
+    spin = getattr(torch.cuda, "_sleep", None)
+
+    def timed(launch, prep=lambda: None):
+        """Mean device time of `launch`; `prep` (state resets) runs outside the events."""
+        for _ in range(3):
+            prep()
+            launch()
+        torch.cuda.synchronize()
+        # a ~20 ms device-side spin first, so that every launch below is queued before the
+        # device reaches it and no event pair includes host-side launch latency
+        if spin is not None:
+            spin(40_000_000)
+        evs = []
+        for _ in range(reps):
+            flush.fill_(1)
+            clean.sum()   # reads 256 MiB: the dirty lines of the write leave L2 before the launch
+            prep()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        assert td.td_device_error() == 0
+        return sum(a.elapsed_time(b) for a, b in evs) / reps
+
+    for L in (512, 2048, 8192, 32768):
+        wl = synth.attention_sweep(L, dev, B=32)
+        lay, dims = wl.layers[0], wl.dims.as_dict()
+        ws = td.workspace(dims, td.TD_FN_BLOCK_ATTENTION, dev)
+        o = torch.empty_like(lay["q"])
+        ms = timed(lambda: td.td_block_attention(dims, lay["q"], lay["k_blk"], lay["v_blk"],
+                                                 lay["k_ctx"], lay["v_ctx"], o=o, ws=ws))
+        dm = wl.dims
+        nbytes = 2 * dm.B * dm.Hkv * dm.Lmax * dm.D * 2 + (
+            lay["q"].numel() + o.numel() + lay["k_blk"].numel() + lay["v_blk"].numel()) * 2
+        gbs = nbytes / (ms / 1e3) / 1e9
+        flops = 4.0 * dm.B * dm.Hq * dm.S * (dm.Lmax + dm.S) * dm.D
+        print(json.dumps({"sweep": "attention", "B": dm.B, "L": L, "ms": round(ms, 4),
+                          "algorithmic_bytes": nbytes, "GB/s": round(gbs, 1),
+                          "hbm_frac": round(gbs / pk["hbm_gbs"], 4),
+                          "TFLOP/s": round(flops / (ms / 1e3) / 1e12, 1),
+                          "peak_source": pk_kind}), flush=True)
+        del wl, lay, ws, o
+        torch.cuda.empty_cache()
+
+    for M in (16, 256, 1024, 4096):
+        wl = synth.lmhead_sweep(M, 16, 0.8, dev)
+        dims = wl.dims.as_dict()
+        ws = td.workspace(dims, td.TD_FN_LMHEAD_COMMIT, dev)
+        dm = wl.dims
+
+        def reset():
+            wl.tokens.fill_(dm.V)
+            wl.masked.fill_(1)
+
+        ms = timed(lambda: td.td_lmhead_commit(dims, wl.h, wl.w_lm, 0.8, False, wl.tokens,
+                                               wl.masked, ws=ws), reset)
+        flops = 2.0 * M * dm.d * dm.V
+        nbytes = (dm.V * dm.d + M * dm.d) * 2
+        tf = flops / (ms / 1e3) / 1e12
+        gbs = nbytes / (ms / 1e3) / 1e9
+        print(json.dumps({"sweep": "lmhead_commit", "M": M, "S": 16, "ms": round(ms, 4),
+                          "TFLOP/s": round(tf, 1), "tensor_frac": round(tf / pk["bf16_tflops"], 4),
+                          "GB/s": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 4),
+                          "peak_source": pk_kind}), flush=True)
+        del wl, ws
+        torch.cuda.empty_cache()
 
 
 def run_reference(args, world, rank):
