@@ -148,8 +148,11 @@ const char* td_status_string(td_status s);
  *   x_hat = (h_r - mean(h_r)) / sqrt(var(h_r) + eps)   (population variance, no affine)
  *   x_mod_r = bf16(x_hat * (1 + m[1]) + m[0])
  * h: bf16 [rows, d] (read only). x_mod: bf16 [rows, d] (written). No workspace.
- * Errors: TD_ERR_INVALID_ARG (null, rows <= 0, d <= 0, eps < 0), TD_ERR_UNSUPPORTED
- * (d % 8 != 0). */
+ * Statistics in fp32. h and x_mod start on 16-byte boundaries; E and phi need only fp32
+ * alignment (d % 256 == 0 with 16-byte aligned E and phi takes the vectorised kernel, any
+ * other case a scalar one; both give the same result up to fp32 rounding).
+ * Errors: TD_ERR_INVALID_ARG (null, rows <= 0, d <= 0, eps < 0, h or x_mod not 16-byte
+ * aligned), TD_ERR_UNSUPPORTED (d % 8 != 0 or d > 8192). */
 td_status td_adaln_modulate(const void* h, const float* E, const float* phi, int rows, int d,
                             float eps, void* x_mod, void* stream);
 

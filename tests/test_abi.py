@@ -111,3 +111,13 @@ def test_malformed_paging_is_rejected(lib):
         assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None,
                                       ctypes.byref(pg), fake, None, fake, 1 << 30, None) == 1
         assert lib.td_kv_append(ctypes.byref(dm), None, None, fake, ctypes.byref(pg), None) == 1
+
+
+def test_adaln_shape_and_alignment_checks(lib):
+    fake = ctypes.c_void_p(1 << 40)        # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p((1 << 40) + 2)   # bf16-aligned but off a 16-byte boundary
+    assert lib.td_adaln_modulate(fake, fake, fake, 4, 8200, 1e-6, fake, None) == 3   # d > 8192
+    assert lib.td_adaln_modulate(fake, fake, fake, 4, 260, 1e-6, fake, None) == 3    # d % 8
+    assert lib.td_adaln_modulate(odd, fake, fake, 4, 256, 1e-6, fake, None) == 1
+    assert lib.td_adaln_modulate(fake, fake, fake, 4, 256, 1e-6, odd, None) == 1
+    assert lib.td_adaln_modulate(fake, fake, fake, 4, 256, -1.0, fake, None) == 1     # eps < 0
