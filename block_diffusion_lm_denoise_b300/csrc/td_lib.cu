@@ -592,56 +592,59 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
   }
   u(ctx_len); u(emb); u(pos); u(w_lm); u(phi_table); u(tokens); u(masked); u(conf); u(pred);
   u(n_committed); u(all_done); u(ws);
-  cudaGraphExec_t exec = nullptr;
   {
+    // One lock over lookup, capture, insertion and launch: no two threads capture on the
+    // shared capture stream at once, a key is captured once, and no graph is destroyed
+    // between its lookup and its launch (eviction synchronizes the device first, so launches
+    // already queued finish before their graph goes).
     std::lock_guard<std::mutex> lk(g_loop_mu);
+    cudaGraphExec_t exec = nullptr;
     auto it = g_loop_graphs.find(key);
     if (it != g_loop_graphs.end()) exec = it->second;
-  }
-  if (exec == nullptr) {
-    set_all_smem();
-    cudaStream_t cs = capture_stream();
-    if (cs == nullptr) return TD_ERR_UNSUPPORTED;
-    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
-      cudaGetLastError();
-      return TD_ERR_UNSUPPORTED;
-    }
-    td_status s = TD_OK;
-    if (cudaMemsetAsync(all_done, 0, sizeof(int), cs) != cudaSuccess ||
-        cudaMemsetAsync(w.loop, 0, sizeof(int), cs) != cudaSuccess)
-      s = TD_ERR_CUDA;
-    for (int t = t_start; t <= T && s == TD_OK; ++t)
-      s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
-                   phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, rope_theta,
-                   paging, tokens, masked, conf, pred, n_committed, all_done, ws, cs, nsm,
-                   all_done, w.loop);
-    cudaGraph_t g = nullptr;
-    const cudaError_t ee = cudaStreamEndCapture(cs, &g);
-    if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
-      if (g) cudaGraphDestroy(g);
-      cudaGetLastError();
-      return s != TD_OK ? s : TD_ERR_UNSUPPORTED;
-    }
-    const cudaError_t ie = cudaGraphInstantiate(&exec, g, 0);
-    cudaGraphDestroy(g);
-    if (ie != cudaSuccess) {
-      cudaGetLastError();
-      return TD_ERR_UNSUPPORTED;
-    }
-    std::lock_guard<std::mutex> lk(g_loop_mu);
-    g_loop_graphs[key] = exec;
-    g_loop_order.push_back(key);
-    if (g_loop_order.size() > kMaxLoopGraphs) {
-      auto old = g_loop_graphs.find(g_loop_order.front());
-      if (old != g_loop_graphs.end()) {
-        cudaDeviceSynchronize();
-        cudaGraphExecDestroy(old->second);
-        g_loop_graphs.erase(old);
+    if (exec == nullptr) {
+      set_all_smem();
+      cudaStream_t cs = capture_stream();
+      if (cs == nullptr) return TD_ERR_UNSUPPORTED;
+      if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        return TD_ERR_UNSUPPORTED;
       }
-      g_loop_order.erase(g_loop_order.begin());
+      td_status s = TD_OK;
+      if (cudaMemsetAsync(all_done, 0, sizeof(int), cs) != cudaSuccess ||
+          cudaMemsetAsync(w.loop, 0, sizeof(int), cs) != cudaSuccess)
+        s = TD_ERR_CUDA;
+      for (int t = t_start; t <= T && s == TD_OK; ++t)
+        s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
+                     phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, rope_theta,
+                     paging, tokens, masked, conf, pred, n_committed, all_done, ws, cs, nsm,
+                     all_done, w.loop);
+      cudaGraph_t g = nullptr;
+      const cudaError_t ee = cudaStreamEndCapture(cs, &g);
+      if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
+        if (g) cudaGraphDestroy(g);
+        cudaGetLastError();
+        return s != TD_OK ? s : TD_ERR_UNSUPPORTED;
+      }
+      const cudaError_t ie = cudaGraphInstantiate(&exec, g, 0);
+      cudaGraphDestroy(g);
+      if (ie != cudaSuccess) {
+        cudaGetLastError();
+        return TD_ERR_UNSUPPORTED;
+      }
+      g_loop_graphs[key] = exec;
+      g_loop_order.push_back(key);
+      if (g_loop_order.size() > kMaxLoopGraphs) {
+        auto old = g_loop_graphs.find(g_loop_order.front());
+        if (old != g_loop_graphs.end()) {
+          cudaDeviceSynchronize();
+          cudaGraphExecDestroy(old->second);
+          g_loop_graphs.erase(old);
+        }
+        g_loop_order.erase(g_loop_order.begin());
+      }
     }
+    TD_CUDA(cudaGraphLaunch(exec, st));
   }
-  TD_CUDA(cudaGraphLaunch(exec, st));
   int host[2] = {0, 0};
   TD_CUDA(cudaMemcpyAsync(&host[0], w.loop, sizeof(int), cudaMemcpyDeviceToHost, st));
   TD_CUDA(cudaMemcpyAsync(&host[1], all_done, sizeof(int), cudaMemcpyDeviceToHost, st));

@@ -344,3 +344,63 @@ def test_paged_attention_at_full_size_is_bit_identical_to_contiguous(cuda_device
     torch.cuda.synchronize()
     assert td.td_device_error() == 0
     assert torch.equal(o_c, o_p)
+
+
+
+def test_decode_loops_from_four_threads_match_one_thread(cuda_device):
+    # Four host threads run the block decode loop at once, each on its own stream with its
+    # own state and workspace (so each captures a graph of its own): every result equals the
+    # one of the same loop run alone, and repeated calls (cached graphs) agree too.
+    import threading
+    dm = synth.Dims(B=2, S=16, d=256, Hq=8, Hkv=2, D=128, V=2048, Lmax=100, n_layers=2)
+    layers, w_lm, emb, pos, phi = _small_model(71, dm, cuda_device, w_scale=0.08)
+    ctx = torch.tensor([100, 41], dtype=torch.int32, device=cuda_device)
+
+    def state():
+        return dict(tokens=torch.full((dm.B, dm.S), dm.V, dtype=torch.int32, device=cuda_device),
+                    masked=torch.ones((dm.B, dm.S), dtype=torch.uint8, device=cuda_device),
+                    ws=td.workspace(dm.as_dict(), td.TD_FN_DECODE_BLOCK, cuda_device),
+                    outs=td._outs(dm.B, dm.S, cuda_device, None, None, None, None),
+                    stream=torch.cuda.Stream(cuda_device))
+
+    def decode(st):
+        with torch.cuda.stream(st["stream"]):   # ordered before the loop on its stream
+            st["tokens"].fill_(dm.V)
+            st["masked"].fill_(1)
+        c, p, n, a = st["outs"]
+        return td.td_decode_block(dm.as_dict(), layers, emb, pos, w_lm, phi, dm.S, 0.8,
+                                  st["tokens"], st["masked"], ctx_len=ctx, conf=c, pred=p,
+                                  n_committed=n, all_done=a, ws=st["ws"], stream=st["stream"])
+
+    alone = state()
+    steps_ref = decode(alone)
+    tokens_ref = alone["tokens"].clone()
+    assert td.td_device_error() == 0 and not alone["masked"].any()
+
+    states = [state() for _ in range(4)]
+    results, errors = [None] * 4, []
+
+    def worker(i):
+        try:
+            runs = []
+            for _ in range(3):
+                steps = decode(states[i])
+                runs.append((steps, states[i]["tokens"].clone(), states[i]["masked"].clone()))
+            results[i] = runs
+        except Exception as e:   # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert td.td_device_error() == 0
+    for runs in results:
+        assert runs is not None
+        for steps, tokens, masked in runs:
+            assert steps == steps_ref
+            assert torch.equal(tokens, tokens_ref)
+            assert not masked.any()
