@@ -380,7 +380,9 @@ def test_brute_force_step_on_tiny_inputs():
     d, Hq, Hkv, D, S, L = dm.d, dm.Hq, dm.Hkv, dm.D, dm.S, dm.Lmax
     ph = oracle.as_f64(phi[0])
     tokens = np.array([[dm.V, 3]])
-    h = oracle.embed(tokens, emb, pos)
+    ef, pf = oracle.as_f64(emb), oracle.as_f64(pos)
+    h = np.array([[oracle.bf16_round(ef[tokens[0, i], c] + pf[i, c]) for c in range(dm.d)]
+                  for i in range(S)])
     m = lay["ada_E"] + ph
     xm = np.zeros_like(h)
     for r in range(S):
@@ -418,6 +420,26 @@ def test_brute_force_step_on_tiny_inputs():
         cf = 1.0 / sum(math.exp(zz - zm) for zz in z[rr])
         assert abs(cf - r["conf"][0, rr]) < 1e-6
         assert z[rr].index(zm) == r["pred"][0, rr]
+
+
+def test_embed_gathers_token_rows_and_adds_the_position_of_the_block_slot():
+    # two sequences, so a position indexed by sequence instead of block slot would show;
+    # the [MASK] id V reads the extra last row of the table
+    V, S, d = 5, 3, 4
+    rng = np.random.default_rng(8)
+    emb = rng.standard_normal((V + 1, d))
+    pos = rng.standard_normal((S, d))
+    tokens = np.array([[V, 0, 4], [2, V, 2]])
+    h = oracle.embed(tokens, emb, pos)
+    assert h.shape == (2 * S, d)
+    for b in range(2):
+        for i in range(S):
+            for c in range(d):
+                assert h[b * S + i, c] == oracle.bf16_round(emb[tokens[b, i], c] + pos[i, c])
+    # the sum is rounded once: bf16(e + p), not bf16(e) + bf16(p)
+    e1 = np.zeros((V + 1, 1)); e1[0, 0] = 1.0
+    p1 = np.array([[2.0 ** -9], [0.0], [0.0]])
+    assert oracle.embed(np.array([[0, 1, 1]]), e1, p1)[0, 0] == oracle.bf16_round(1.0 + 2.0 ** -9)
 
 
 # ----------------------------------------------------------------------------- mock-AR reading
