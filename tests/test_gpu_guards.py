@@ -50,6 +50,8 @@ SHAPES = [
     (2, 4, 8, 2, 64, 130, [130, 5]),           # tiny block, ragged context past one tile
     (1, 32, 32, 2, 128, 257, None),            # S = 32: 512 query rows per KV head
     (3, 16, 32, 2, 128, 383, [383, 0, 129]),   # SM pairs, three tiles, empty and ragged
+    (2, 64, 8, 2, 128, 200, [200, 63]),        # the largest block, S = 64
+    (1, 48, 32, 2, 128, 129, None),            # S = 48: 96-row chunks on SM pairs
 ]
 
 

@@ -71,6 +71,9 @@ ATTN_CASES = [
     (1, 1, 4, 1, 64, 0, None),                # one key: output == v exactly
     (3, 16, 32, 2, 128, 4000, [4000, 1234, 0]),  # split-K: several tiles and units per team
     (4, 16, 16, 4, 64, 2000, None),           # D = 64 with split-K and four KV heads
+    (2, 64, 32, 2, 128, 300, [300, 45]),      # the largest block, S = 64: 8 chunks per unit
+    (2, 48, 32, 2, 128, 260, None),           # S = 48: 96-row chunks on SM pairs
+    (1, 5, 8, 2, 64, 130, None),              # odd S: one 20-row chunk per KV head
 ]
 
 
