@@ -780,6 +780,9 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
   if (!w_lm || !phi_t || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
     return TD_ERR_INVALID_ARG;
   if (!h && (!emb || !pos)) return TD_ERR_INVALID_ARG;
+  // emb / pos are read in 16-byte vectors, w_lm through a tensor map
+  if (!aligned16(w_lm) || (!h && (!aligned16(emb) || !aligned16(pos))))
+    return TD_ERR_INVALID_ARG;
   if (t < 1 || T < 1 || t > T || std::isnan(gamma)) return TD_ERR_INVALID_ARG;
   const int nsm = sm_count();
   if (!ws_ok(ws, ws_bytes, carve_step(dims, nullptr, nsm).total)) return TD_ERR_WORKSPACE;
@@ -804,6 +807,7 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   if (!emb || !pos || !w_lm || !phi_table || !tokens || !masked || !conf || !pred ||
       !n_committed || !all_done || !steps_taken)
     return TD_ERR_INVALID_ARG;
+  if (!aligned16(w_lm) || !aligned16(emb) || !aligned16(pos)) return TD_ERR_INVALID_ARG;
   if (t_start < 1 || T < 1 || std::isnan(gamma)) return TD_ERR_INVALID_ARG;
   const int nsm = sm_count();
   if (!ws_ok(ws, ws_bytes, carve_step(dims, nullptr, nsm).total)) return TD_ERR_WORKSPACE;

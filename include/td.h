@@ -215,7 +215,10 @@ td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm,
  * LM head reads their count on the device). Rows not evaluated get conf = 0 and pred = -1.
  *   phi_t fp32 [6, d]: the shared adaLN-single timestep vector of step t (1 <= t <= T).
  *   layers: HOST array of dims->n_layers td_layer structs (device pointers inside).
- *   ctx_len int32 [B] device or NULL.  Other outputs as in td_lmhead_commit. */
+ *   ctx_len int32 [B] device or NULL.  Other outputs as in td_lmhead_commit.
+ * Errors: TD_ERR_INVALID_ARG also when w_lm, or (on the embedding path) emb or pos, does
+ * not start on a 16-byte boundary, or when a layer's weights, table or caches do not; h
+ * may have any 2-byte alignment (it is copied into the workspace first). */
 td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* h, const void* emb, const void* pos, const void* w_lm,
                           const float* phi_t, int t, int T, float gamma,
@@ -235,7 +238,8 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
  * the host once per block (plus one read of `masked` on entry). If capture is not possible
  * the steps run from a host loop that reads all_done back after each step.
  * Returns TD_ERR_NOT_CONVERGED only if positions remain masked after step T (cannot
- * happen with force-commit at t == T; kept for callers that stop early). */
+ * happen with force-commit at t == T; kept for callers that stop early). Alignment rules and
+ * the other errors as in td_denoise_step (emb and pos are always read here). */
 td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
                           const void* emb, const void* pos, const void* w_lm,
                           const float* phi_table, int t_start, int T, float gamma,

@@ -121,3 +121,22 @@ def test_adaln_shape_and_alignment_checks(lib):
     assert lib.td_adaln_modulate(odd, fake, fake, 4, 256, 1e-6, fake, None) == 1
     assert lib.td_adaln_modulate(fake, fake, fake, 4, 256, 1e-6, odd, None) == 1
     assert lib.td_adaln_modulate(fake, fake, fake, 4, 256, -1.0, fake, None) == 1     # eps < 0
+
+
+def test_step_and_loop_reject_misaligned_tables_before_any_launch(lib):
+    dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=0, n_layers=0)
+    fake = ctypes.c_void_p(1 << 40)        # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p((1 << 40) + 2)   # bf16-aligned but off a 16-byte boundary
+    steps = ctypes.c_int(0)
+    for emb, pos, w in ((odd, fake, fake), (fake, odd, fake), (fake, fake, odd)):
+        # embedding path (h = NULL)
+        assert lib.td_denoise_step(ctypes.byref(dm), None, None, None, emb, pos, w, fake, 1,
+                                   16, 0.8, None, fake, fake, fake, fake, fake, fake, fake,
+                                   1 << 30, None) == 1
+        assert lib.td_decode_block(ctypes.byref(dm), None, None, emb, pos, w, fake, 1, 16,
+                                   0.8, None, fake, fake, fake, fake, fake, fake,
+                                   ctypes.byref(steps), fake, 1 << 30, None) == 1
+    # with h given, emb / pos are not read and may be anything; w_lm still must be aligned
+    assert lib.td_denoise_step(ctypes.byref(dm), None, None, odd, None, None, odd, fake, 1, 16,
+                               0.8, None, fake, fake, fake, fake, fake, fake, fake, 1 << 30,
+                               None) == 1
