@@ -394,7 +394,9 @@ def main():
                "share_of_step": round(lm_share, 3), "peak_source": pk_kind}
     dominant, other = (roof_attn, roof_lm) if attn_share >= lm_share else (roof_lm, roof_attn)
 
-    # embed, LM row map, 6 x (adaLN, QKV, attention, O-proj), LM head, commit
+    # embed, LM row map, 6 x (adaLN, QKV, attention, O-proj), LM head, commit; the block's
+    # graph holds the kernels of all T steps and launches every one of them (those after the
+    # step that finished the block return at once)
     launches_per_step = 2 + dm.n_layers * 4 + 2
     result = {
         "metric": "committed tokens/sec (block decode, S=16, gamma=0.8)",
@@ -414,7 +416,7 @@ def main():
         "denoised_tokens_per_s": round(denoised, 1),
         "denoise_steps_per_block": round(total_steps / args.steps, 3),
         "commit_sweep": sweep,
-        "gpu_launches": launches_per_step * total_steps,
+        "gpu_launches": launches_per_step * wl.T * args.steps,
         "clocks": clocks.summary(),
         "roofline": dominant,
         "roofline_other": other,
