@@ -31,6 +31,11 @@
  *   - Shapes supported by the kernels: D in {64, 128}; Hq % Hkv == 0; 1 <= S <= 64;
  *     d % 64 == 0 (and d <= 8192 for the denoise step); V % 8 == 0; B*S <= 65536;
  *     Lmax >= 0.
+ *   - Host threads may call into the library at the same time when their calls use
+ *     distinct output and workspace buffers (td_lmhead_commit_static is the exception: all
+ *     its calls share one scratch array). The host-side caches (shared-memory opt-ins, the
+ *     captured decode graphs) are guarded by locks. The device error word is one per device,
+ *     shared by every caller.
  */
 #ifndef TD_H_
 #define TD_H_
