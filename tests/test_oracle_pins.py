@@ -236,6 +236,34 @@ def test_attention_key_permutation_invariance_and_lse_merge_identity():
 
 # ----------------------------------------------------------------------------- LM head
 
+def test_attention_matches_torch_sdpa_with_concatenated_keys_and_repeated_kv_heads():
+    # the library routine, in fp64, on the keys ctx[:L_b] ++ block with each KV head
+    # repeated for its G = Hq / Hkv consecutive query heads; lse from torch.logsumexp
+    import torch
+    gen = np.random.default_rng(17)
+    B, S, Hq, Hkv, D, Lmax = 3, 5, 6, 2, 16, 9
+    q = gen.standard_normal((B, S, Hq, D)); kb = gen.standard_normal((B, S, Hkv, D))
+    vb = gen.standard_normal((B, S, Hkv, D))
+    kc = gen.standard_normal((B, Hkv, Lmax, D)); vc = gen.standard_normal((B, Hkv, Lmax, D))
+    ctx = [9, 0, 4]
+    o, lse = oracle.block_attention(q, kb, vb, kc, vc, ctx)
+    G = Hq // Hkv
+    for b in range(B):
+        L = ctx[b]
+        keys = torch.cat([torch.from_numpy(kc[b, :, :L]), torch.from_numpy(kb[b]).transpose(0, 1)],
+                         dim=1)                                  # [Hkv, L + S, D]
+        vals = torch.cat([torch.from_numpy(vc[b, :, :L]), torch.from_numpy(vb[b]).transpose(0, 1)],
+                         dim=1)
+        keys = keys.repeat_interleave(G, dim=0)                  # [Hq, L + S, D]
+        vals = vals.repeat_interleave(G, dim=0)
+        qq = torch.from_numpy(q[b]).transpose(0, 1)              # [Hq, S, D]
+        ref = torch.nn.functional.scaled_dot_product_attention(qq, keys, vals)
+        assert np.allclose(o[b], ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+        sc = qq @ keys.transpose(1, 2) / math.sqrt(D)
+        assert np.allclose(lse[b], torch.logsumexp(sc, dim=-1).transpose(0, 1).numpy(),
+                           rtol=1e-12, atol=1e-12)
+
+
 def test_lmhead_zero_weights_give_uniform_confidence_exactly():
     V, d = 1024, 64
     h = bf16_exact((3, d))
