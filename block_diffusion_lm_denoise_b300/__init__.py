@@ -122,6 +122,8 @@ def _stream(stream) -> Optional[int]:
 
 
 def make_dims(B, S, d, Hq, Hkv, D, V, Lmax, n_layers) -> td_dims:
+    """td_dims from its nine sizes (sequences, block size, hidden size, query / KV heads,
+    head dim, vocabulary, context capacity, layers)."""
     return td_dims(B, S, d, Hq, Hkv, D, V, Lmax, n_layers)
 
 
@@ -133,6 +135,8 @@ def dims_from(obj) -> td_dims:
 
 
 def td_workspace_size(dims, fn: int) -> int:
+    """Bytes of caller workspace entry point `fn` (a TD_FN_* value) needs at these sizes;
+    raises TdError for sizes the kernels do not support."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     n = lib().td_workspace_size(ctypes.byref(dm), fn)
     if n == ctypes.c_size_t(-1).value:
@@ -158,6 +162,8 @@ def td_device_error() -> int:
 
 def td_adaln_modulate(h: torch.Tensor, E: torch.Tensor, phi: torch.Tensor, eps: float = 1e-6,
                       x_mod: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """x_mod = bf16(LayerNorm(h) * (1 + m[1]) + m[0]) with m = E + phi, for h bf16 [rows, d]
+    and E, phi fp32 [6, d]; returns x_mod (allocated when not given)."""
     rows, d = h.shape
     if x_mod is None:
         x_mod = torch.empty_like(h)
