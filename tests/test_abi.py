@@ -140,3 +140,32 @@ def test_step_and_loop_reject_misaligned_tables_before_any_launch(lib):
     assert lib.td_denoise_step(ctypes.byref(dm), None, None, odd, None, None, odd, fake, 1, 16,
                                0.8, None, fake, fake, fake, fake, fake, fake, fake, 1 << 30,
                                None) == 1
+
+
+def test_static_entry_point_rejects_sizes_beyond_its_scratch_before_any_cuda_call(lib):
+    # 16 MiB of scratch holds the LM-head partials of B*S <= 2048 rows at V = 131072
+    # (12 bytes per row and 256-wide vocabulary tile); beyond that: TD_ERR_WORKSPACE
+    fake = ctypes.c_void_p(1 << 40)        # never dereferenced: the size check fails first
+    big = td.make_dims(B=256, S=16, d=4096, Hq=32, Hkv=2, D=128, V=131072, Lmax=0, n_layers=0)
+    assert lib.td_lmhead_commit_static(ctypes.byref(big), fake, fake, 0.8, 0, fake, fake, fake,
+                                       fake, fake, fake, None) == 2
+    odd = ctypes.c_void_p((1 << 40) + 2)
+    ok = td.make_dims(B=64, S=16, d=4096, Hq=32, Hkv=2, D=128, V=131072, Lmax=0, n_layers=0)
+    assert lib.td_lmhead_commit_static(ctypes.byref(ok), odd, fake, 0.8, 0, fake, fake, fake,
+                                       fake, fake, fake, None) == 1
+
+
+def test_workspace_sizes_grow_with_the_problem():
+    base = dict(B=8, S=16, d=4096, Hq=32, Hkv=2, D=128, V=131072, Lmax=2048, n_layers=2)
+
+    def ws(fn, **kw):
+        return td.td_workspace_size(td.make_dims(**{**base, **kw}), fn)
+
+    for fn in (td.TD_FN_BLOCK_ATTENTION, td.TD_FN_LMHEAD_COMMIT, td.TD_FN_DENOISE_STEP):
+        assert ws(fn, B=16) >= ws(fn, B=8)
+    assert ws(td.TD_FN_LMHEAD_COMMIT, V=262144) > ws(td.TD_FN_LMHEAD_COMMIT)
+    # a step holds the attention's and the LM head's scratch besides its activations
+    step = ws(td.TD_FN_DENOISE_STEP)
+    assert step >= ws(td.TD_FN_LMHEAD_COMMIT) and step >= ws(td.TD_FN_BLOCK_ATTENTION)
+    # the loop runs the step: the same workspace
+    assert ws(td.TD_FN_DECODE_BLOCK) == step
