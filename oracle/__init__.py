@@ -25,4 +25,6 @@ from .td_oracle import (  # noqa: F401
     oproj_gated_residual,
     qkv_project,
     rope_rotate,
+    timestep_embedding,
+    timestep_table,
 )

@@ -42,6 +42,8 @@ notes of the repository):
      masked position of maximal conf; at t == T every masked position commits.
   R7 bf16 storage points: x_mod (Q1), q/k/v (Q2), attention output (Q3), the updated
      hidden state (Q4), and the embedding sum; every other value stays in fp64 here.
+  R19 the timestep map of adaLN-single (optional; the step itself takes phi(t) as input):
+     phi(t) = W_t e(t / T) + b_t, e the 256-wide sinusoidal embedding of 1000 t / T.
 """
 
 from __future__ import annotations
@@ -90,6 +92,36 @@ def adaln_vectors(E, phi):
     """m = E_l + phi(t) in fp64, returned as (shift, scale, gate) rows of length d."""
     m = as_f64(E) + as_f64(phi)
     return m[0], m[1], m[2]
+
+
+TIMESTEP_DIM = 256        # width of the sinusoidal embedding of tau (R19)
+TIMESTEP_SCALE = 1000.0   # tau in (0, 1] is embedded at 1000 tau (R19)
+
+
+def timestep_embedding(tau) -> np.ndarray:
+    """Sinusoidal embedding of the diffusion time tau = t / T (reading R19: the pages name
+    adaLN-single but not its timestep map). With s = 1000 tau and frequencies
+    w_j = 10000^(-j / 128), j = 0..127: e[j] = cos(s w_j), e[128 + j] = sin(s w_j).
+    tau: scalar or [n]; returns [n, 256] (fp64)."""
+    tau = np.atleast_1d(np.asarray(tau, dtype=np.float64))
+    half = TIMESTEP_DIM // 2
+    j = np.arange(half, dtype=np.float64)
+    w = np.power(10000.0, -j / half)
+    arg = (TIMESTEP_SCALE * tau)[:, None] * w[None, :]
+    return np.concatenate([np.cos(arg), np.sin(arg)], axis=1)
+
+
+def timestep_table(w_t, b_t, T: int) -> np.ndarray:
+    """The shared adaLN-single vectors phi(t) for t = 1..T ([chathome] inference paragraph:
+    the diffusion timestep modulates every layer through adaLN-single; reading R19):
+    phi(t) = W_t e(t / T) + b_t with W_t [6d, 256] and b_t [6d] (fp32 parameters), computed
+    in fp64 and returned as [T, 6, d] fp64 (the library stores it rounded to fp32)."""
+    W = as_f64(w_t)
+    b = as_f64(b_t)
+    d6 = W.shape[0]
+    tau = np.arange(1, T + 1, dtype=np.float64) / T
+    e = timestep_embedding(tau)                                  # [T, 256]
+    return (e @ W.T + b[None, :]).reshape(T, 6, d6 // 6)
 
 
 def layer_norm(h) -> np.ndarray:

@@ -570,3 +570,53 @@ def test_block_positions_follow_the_context():
     dims = dict(B=2, S=3, Lmax=50)
     assert list(oracle.block_positions(dims, [7, 0])) == [7, 8, 9, 0, 1, 2]
     assert list(oracle.block_positions(dims)) == [50, 51, 52, 50, 51, 52]
+
+
+# ------------------------------------------------------------------------------ timestep map
+
+def test_timestep_embedding_at_zero_and_unit_pair_norms():
+    # tau = 0: every cosine is 1 and every sine 0 (closed form of the definition)
+    e0 = oracle.timestep_embedding(0.0)[0]
+    assert np.array_equal(e0[:128], np.ones(128)) and np.array_equal(e0[128:], np.zeros(128))
+    # any tau: each (cos, sin) pair has unit length, so the embedding's squared norm is 128
+    e = oracle.timestep_embedding(np.array([0.0625, 0.3, 1.0]))
+    pairs = e[:, :128] ** 2 + e[:, 128:] ** 2
+    assert np.allclose(pairs, 1.0, atol=1e-15)
+
+
+def test_timestep_embedding_frequencies_as_complex_exponentials():
+    # e[j] + i e[128 + j] = exp(i 1000 tau 10000^(-j/128)): the lowest index turns fastest (one
+    # radian per 1/1000 of tau), the last slowest; checked against numpy's complex exponential
+    tau = np.array([0.125, 0.5, 0.9375])
+    e = oracle.timestep_embedding(tau)
+    j = np.arange(128)
+    z = np.exp(1j * 1000.0 * tau[:, None] * 10000.0 ** (-j[None, :] / 128.0))
+    assert np.allclose(e[:, :128], z.real, atol=1e-12)
+    assert np.allclose(e[:, 128:], z.imag, atol=1e-12)
+    # j = 0 at tau = pi / 2000: cos = 0, sin = 1
+    q = oracle.timestep_embedding(math.pi / 2000.0)[0]
+    assert abs(q[0]) < 1e-15 and abs(q[128] - 1.0) < 1e-15
+
+
+def test_timestep_table_rows_steps_and_bias():
+    d, T = 8, 4
+    rng = np.random.default_rng(5)
+    W = rng.standard_normal((6 * d, 256))
+    b = rng.standard_normal(6 * d)
+    phi = oracle.timestep_table(W, b, T)
+    assert phi.shape == (T, 6, d)
+    # zero weights: every step's vector is the bias, laid out as 6 rows of d
+    assert np.array_equal(oracle.timestep_table(np.zeros_like(W), b, T),
+                          np.broadcast_to(b.reshape(6, d), (T, 6, d)))
+    # step t uses tau = t / T; a one-hot weight column reads one embedding feature
+    Wj = np.zeros_like(W)
+    Wj[3 * d + 5, 200] = 1.0           # row 3 (of 6), column 5 <- feature 200 = sin(s w_72)
+    got = oracle.timestep_table(Wj, np.zeros(6 * d), T)[:, 3, 5]
+    want = [math.sin(1000.0 * t / T * 10000.0 ** (-72 / 128.0)) for t in range(1, T + 1)]
+    assert np.allclose(got, want, atol=1e-12)
+    # linear in (W, b)
+    W2 = rng.standard_normal((6 * d, 256))
+    b2 = rng.standard_normal(6 * d)
+    lhs = oracle.timestep_table(W + 2.0 * W2, b + 2.0 * b2, T)
+    rhs = phi + 2.0 * oracle.timestep_table(W2, b2, T)
+    assert np.allclose(lhs, rhs, atol=1e-10)
