@@ -6,7 +6,10 @@ S=16, T=16 steps, 6 stacked denoiser attention layers each with its own context-
 cache, d=4096, 32 query / 2 KV heads, head_dim 128, vocabulary 131072, gamma=0.8, bf16.
 One bench step = one td_decode_block call on a fresh all-[MASK] block: embedding, adaLN,
 QKV projection, fused block attention, gated O projection, LM head + commit, repeated until
-every position is committed. Inputs are seeded synthetic tensors created in HBM.
+every position is committed. Inputs are seeded synthetic tensors created in HBM. The LM-head
+weights use the calibrated scale of the workload (logits as sharp as the mid-size step's, so
+several positions clear gamma early in a block); the same block with the plain scale (one
+commit per sequence and step, the 16-step worst case) is timed as well.
 
 value = committed tokens / s (B*S per block / block wall time), whole job over all ranks.
 Also printed: denoised tokens / s (B*S*steps / time), the roofline of the dominant kernel,
@@ -35,6 +38,7 @@ import torch  # noqa: E402
 
 WORKLOAD = dict(workload="block decode loop", B=64, S=16, L=8192, n_layers=6, d=4096, Hq=32,
                 Hkv=2, D=128, V=131072, T=16, gamma=0.8)
+FALLBACK_W_LM_SIGMA = 0.02   # the plain LM-head scale: no position clears any threshold
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0)
 
@@ -139,7 +143,10 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
+    def summary(self, ms=None):
+        """Median SM clock, its maximum and the throttle reasons seen; with the segment's
+        device time `ms`, also time x median clock (kilocycles), which compares segments
+        timed at different clocks."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in getattr(self, "lines", []):
@@ -154,8 +161,11 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if ms is not None and sm:
+            out["kcycles"] = round(ms * statistics.median(sm), 1)
+        return out
 
 
 # ------------------------------------------------------------------------------ oracle sample
@@ -214,6 +224,11 @@ def oracle_sample(wl, seconds_budget: float, max_steps: int):
     return committed / el, torch.get_num_threads(), s.describe(steps), steps
 
 
+def host_cores():
+    """(logical cores of the host, threads the oracle's numerical libraries use)."""
+    return os.cpu_count(), torch.get_num_threads()
+
+
 # ------------------------------------------------------------------------------ main
 
 def main():
@@ -254,7 +269,7 @@ def main():
     td.lib()   # fails loudly if the CUDA library is missing
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = synth.decode_loop(dev, seed=4 + rank)
+    wl = synth.decode_loop(dev, seed=4 + rank, w_lm_sigma=synth.DECODE_W_LM_SIGMA)
     dm = wl.dims
     dims = dm.as_dict()
     M = dm.B * dm.S
@@ -263,10 +278,11 @@ def main():
     masked = torch.empty_like(wl.masked)
     outs = td._outs(dm.B, dm.S, dev, None, None, None, None)
 
-    def one_block():
+    def one_block(w_lm=None):
         tokens.fill_(dm.V)
         masked.fill_(1)
-        return td.td_decode_block(dims, wl.layers, wl.emb, wl.pos, wl.w_lm, wl.phi_table, wl.T,
+        return td.td_decode_block(dims, wl.layers, wl.emb, wl.pos,
+                                  wl.w_lm if w_lm is None else w_lm, wl.phi_table, wl.T,
                                   wl.gamma, tokens, masked, conf=outs[0], pred=outs[1],
                                   n_committed=outs[2], all_done=outs[3], ws=ws)
 
@@ -293,10 +309,34 @@ def main():
     value = world * M * args.steps / (ms_max / 1e3)
     denoised = world * M * total_steps / (ms_max / 1e3)
 
+    # ---------------------------------------------------------------- the plain LM-head scale
+    # the same block with W_lm ~ N(0, 0.02): no confidence clears gamma, one commit per
+    # sequence and step (the fallback), 16 steps per block
+    w_plain = synth.normal((dm.V, dm.d), FALLBACK_W_LM_SIGMA, 4 + rank, "w_lm", dev)
+    for _ in range(2):
+        one_block(w_plain)
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as fclocks:
+        f0.record(stream)
+        fsteps = [one_block(w_plain) for _ in range(args.steps)]
+        f1.record(stream)
+        torch.cuda.synchronize()
+    fms = max_over_ranks(f0.elapsed_time(f1), world)
+    fallback = {"w_lm_sigma": FALLBACK_W_LM_SIGMA,
+                "committed_tokens_per_s": round(world * M * args.steps / (fms / 1e3), 1),
+                "denoised_tokens_per_s": round(world * M * sum(fsteps) / (fms / 1e3), 1),
+                "steps_per_block": round(sum(fsteps) / args.steps, 3),
+                "ms_per_block": round(fms / args.steps, 3),
+                "clocks": fclocks.summary(fms)}
+    del w_plain
+
     # ---------------------------------------------------------------- commit-rule sweep
     # steps per block and committed tokens/s of one block at other thresholds and under the
     # left-to-right rule (the pages: lower gamma commits more per step; mock-AR one per step)
     sweep = []
+    hist = None
     for g, rule in ((0.5 / dm.V, td.TD_COMMIT_CONFIDENCE), (0.5, td.TD_COMMIT_CONFIDENCE),
                     (0.8, td.TD_COMMIT_CONFIDENCE), (0.95, td.TD_COMMIT_CONFIDENCE),
                     (0.8, td.TD_COMMIT_LEFT_TO_RIGHT)):
@@ -316,6 +356,22 @@ def main():
         sweep.append({"gamma": g, "rule": "left_to_right" if rule else "confidence",
                       "steps_per_block": st, "commits_per_step": round(M / st, 2),
                       "committed_tokens_per_s": round(world * M / (bms / 1e3), 1)})
+
+    # ---------------------------------------------------------------- commits per step
+    # one block of the headline configuration step by step: positions committed at each step
+    # (all sequences), from td_denoise_step's per-sequence counts
+    sws = td.workspace(dims, td.TD_FN_DENOISE_STEP, dev)
+    tokens.fill_(dm.V)
+    masked.fill_(1)
+    hist = []
+    for t in range(1, wl.T + 1):
+        _, _, ncm, dn = td.td_denoise_step(dims, wl.layers, wl.w_lm, wl.phi_table[t - 1], t,
+                                           wl.T, wl.gamma, tokens, masked, emb=wl.emb,
+                                           pos=wl.pos, ws=sws)
+        hist.append(int(ncm.sum().item()))
+        if int(dn.item()):
+            break
+    del sws
 
     # ---------------------------------------------------------------- end to end (host buffers)
     tok_h = torch.full((dm.B, dm.S), dm.V, dtype=torch.int32).pin_memory()
@@ -337,7 +393,6 @@ def main():
 
     # ---------------------------------------------------------------- roofline (isolated kernels)
     pk, pk_kind = peaks()
-    reps = 10
     lay = wl.layers[0]
     q = synth.normal((dm.B, dm.S, dm.Hq, dm.D), 1.0, 99, "bench.q", dev)
     kb = synth.normal((dm.B, dm.S, dm.Hkv, dm.D), 1.0, 99, "bench.kb", dev)
@@ -346,13 +401,34 @@ def main():
     aws = td.workspace(dims, td.TD_FN_BLOCK_ATTENTION, dev)
     for _ in range(3):
         td.td_block_attention(dims, q, kb, vb, lay["k_ctx"], lay["v_ctx"], o=o, ws=aws)
+    # back-to-back launches for about half a second, so that the clock sampler (50 ms period)
+    # sees the segment; the context K/V (537 MB) is larger than L2
+    a_reps = 3000
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(reps):
-        td.td_block_attention(dims, q, kb, vb, lay["k_ctx"], lay["v_ctx"], o=o, ws=aws)
-    a1.record(stream)
     torch.cuda.synchronize()
-    attn_ms = a0.elapsed_time(a1) / reps
+    with ClockSampler(local) as aclocks:
+        a0.record(stream)
+        for _ in range(a_reps):
+            td.td_block_attention(dims, q, kb, vb, lay["k_ctx"], lay["v_ctx"], o=o, ws=aws)
+        a1.record(stream)
+        torch.cuda.synchronize()
+    attn_ms = a0.elapsed_time(a1) / a_reps
+    # the same launches with the probabilities carried as hi + lo bf16 pairs (a second P V
+    # product per key tile): the cost of the more exact arithmetic
+    s_reps = 1000
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        td.td_block_attention(dims, q, kb, vb, lay["k_ctx"], lay["v_ctx"], o=o, ws=aws,
+                              precision=td.TD_ATTN_P_SPLIT)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as sclocks:
+        b0.record(stream)
+        for _ in range(s_reps):
+            td.td_block_attention(dims, q, kb, vb, lay["k_ctx"], lay["v_ctx"], o=o, ws=aws,
+                                  precision=td.TD_ATTN_P_SPLIT)
+        b1.record(stream)
+        torch.cuda.synchronize()
+    split_ms = b0.elapsed_time(b1) / s_reps
     kv_bytes = 2 * dm.B * dm.Hkv * dm.Lmax * dm.D * 2
     attn_bytes = kv_bytes + (q.numel() + o.numel() + kb.numel() + vb.numel()) * 2
     attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9
@@ -364,13 +440,16 @@ def main():
     for _ in range(3):
         tk.fill_(dm.V); mk.fill_(1)
         td.td_lmhead_commit(dims, h, wl.w_lm, wl.gamma, False, tk, mk, *outs, ws=lws)
+    l_reps = 700
     l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    l0.record(stream)
-    for _ in range(reps):
-        td.td_lmhead_commit(dims, h, wl.w_lm, wl.gamma, False, tk, mk, *outs, ws=lws)
-    l1.record(stream)
     torch.cuda.synchronize()
-    lm_ms = l0.elapsed_time(l1) / reps
+    with ClockSampler(local) as lclocks:
+        l0.record(stream)
+        for _ in range(l_reps):
+            td.td_lmhead_commit(dims, h, wl.w_lm, wl.gamma, False, tk, mk, *outs, ws=lws)
+        l1.record(stream)
+        torch.cuda.synchronize()
+    lm_ms = l0.elapsed_time(l1) / l_reps
     lm_flops = 2.0 * M * dm.d * dm.V
     lm_tflops = lm_flops / (lm_ms / 1e3) / 1e12
     step_ms = ms / max(1, total_steps)
@@ -386,12 +465,14 @@ def main():
                  "achieved": round(attn_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                  "frac": round(attn_gbs / pk["hbm_gbs"], 4), "traffic": attn_traffic,
                  "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(attn_ms, 4),
-                 "share_of_step": round(attn_share, 3), "peak_source": pk_kind}
+                 "share_of_step": round(attn_share, 3), "peak_source": pk_kind,
+                 "clocks": aclocks.summary(attn_ms * a_reps)}
     roof_lm = {"kernel": lm_kernel + " + merge_commit", "bound": "tensor",
                "achieved": round(lm_tflops, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                "frac": round(lm_tflops / pk["bf16_tflops"], 4), "traffic": lm_traffic,
                "algorithmic_flops_per_launch": lm_flops, "ms_per_launch": round(lm_ms, 4),
-               "share_of_step": round(lm_share, 3), "peak_source": pk_kind}
+               "share_of_step": round(lm_share, 3), "peak_source": pk_kind,
+               "clocks": lclocks.summary(lm_ms * l_reps)}
     dominant, other = (roof_attn, roof_lm) if attn_share >= lm_share else (roof_lm, roof_attn)
 
     # embed, LM row map, 6 x (adaLN, QKV, attention, O-proj), LM head, commit; the block's
@@ -411,13 +492,20 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights and context KV of the stated shapes)",
-        "config": dict(WORKLOAD, parallelism=f"replicas x{world}",
+        "config": dict(WORKLOAD, w_lm_sigma=synth.DECODE_W_LM_SIGMA,
+                       parallelism=f"replicas x{world}",
                        l2="inputs larger than L2 (3.2 GB of context KV + 1 GB LM head per step)"),
         "denoised_tokens_per_s": round(denoised, 1),
         "denoise_steps_per_block": round(total_steps / args.steps, 3),
+        "commits_per_step": hist,
+        "fallback_only": fallback,
+        "attention_split_p": {"ms_per_launch": round(split_ms, 4),
+                              "GB/s": round(attn_bytes / (split_ms / 1e3) / 1e9, 1),
+                              "frac": round(attn_bytes / (split_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                              "clocks": sclocks.summary(split_ms * s_reps)},
         "commit_sweep": sweep,
         "gpu_launches": launches_per_step * wl.T * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(ms),
         "roofline": dominant,
         "roofline_other": other,
         "e2e": {"value": round(e2e, 1), "unit": "tokens/s",
@@ -425,8 +513,10 @@ def main():
                 "d2h_bytes_per_step": tok_out.numel() * 4},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, desc, _ = oracle_sample(wl, args.cpu_budget, 64)
-        result["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": cores,
+        v, threads, desc, _ = oracle_sample(wl, args.cpu_budget, 64)
+        ncpu, _ = host_cores()
+        result["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": threads,
+                                  "host_logical_cores": ncpu, "oracle_threads": threads,
                                   "kind": "oracle", "sample": desc}
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -576,7 +666,7 @@ def run_reference(args, world, rank):
         return
     from block_diffusion_lm_denoise_b300 import synth
     dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
-    wl = synth.decode_loop(dev, seed=4)
+    wl = synth.decode_loop(dev, seed=4, w_lm_sigma=synth.DECODE_W_LM_SIGMA)
     smp = OracleSampler(wl)
     for _ in range(args.warmup):
         smp.step()
@@ -600,9 +690,11 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": dict(WORKLOAD, parallelism="host cores"),
+        "config": dict(WORKLOAD, w_lm_sigma=synth.DECODE_W_LM_SIGMA, parallelism="host cores"),
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s",
-                         "cores": torch.get_num_threads(), "kind": "oracle",
+                         "cores": torch.get_num_threads(),
+                         "host_logical_cores": os.cpu_count(),
+                         "oracle_threads": torch.get_num_threads(), "kind": "oracle",
                          "sample": smp.describe(args.steps)},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -25,10 +25,14 @@ TD_FN_DECODE_BLOCK = 4
 TD_COMMIT_CONFIDENCE = 0      # mask-diffusion: confidence masking with threshold gamma
 TD_COMMIT_LEFT_TO_RIGHT = 1   # mock-AR reading: one commit per step, lowest masked index
 
+TD_ATTN_P_BF16 = 0    # attention probabilities rounded to bf16 for the P V product (default)
+TD_ATTN_P_SPLIT = 1   # carried as a hi + lo pair of bf16 values (a second P V product)
+
 # Every symbol the header declares (checked by the tests).
 EXPORTED = ("td_workspace_size", "td_status_string", "td_adaln_modulate", "td_block_attention",
             "td_lmhead_commit", "td_denoise_step", "td_decode_block", "td_device_error",
-            "td_lmhead_commit_static", "td_kv_append", "td_check_bounded_wait")
+            "td_lmhead_commit_static", "td_kv_append", "td_check_bounded_wait",
+            "td_timestep_table")
 
 
 class TdError(RuntimeError):
@@ -53,7 +57,8 @@ class td_paging(ctypes.Structure):
 
 
 class td_step_opts(ctypes.Structure):
-    _fields_ = [("rule", ctypes.c_int), ("rope_theta", ctypes.c_float), ("paging", td_paging)]
+    _fields_ = [("rule", ctypes.c_int), ("rope_theta", ctypes.c_float), ("paging", td_paging),
+                ("h_out", ctypes.c_void_p), ("attn_precision", ctypes.c_int)]
 
 
 class td_kv(ctypes.Structure):
@@ -78,7 +83,7 @@ def lib() -> ctypes.CDLL:
         L.td_status_string.restype = ctypes.c_char_p
         L.td_adaln_modulate.argtypes = [vp, vp, vp, i, i, f, vp, vp]
         L.td_block_attention.argtypes = [ctypes.POINTER(td_dims), vp, vp, vp, vp, vp, vp,
-                                         ctypes.POINTER(td_paging), vp, vp, vp, sz, vp]
+                                         ctypes.POINTER(td_paging), i, vp, vp, vp, sz, vp]
         L.td_lmhead_commit.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, i, vp, vp, vp, vp,
                                        vp, vp, vp, sz, vp]
         L.td_denoise_step.argtypes = [ctypes.POINTER(td_dims), ctypes.POINTER(td_layer), vp, vp,
@@ -91,6 +96,7 @@ def lib() -> ctypes.CDLL:
                                    ctypes.POINTER(td_kv), vp, ctypes.POINTER(td_paging), vp]
         L.td_device_error.argtypes = [ctypes.POINTER(i)]
         L.td_check_bounded_wait.argtypes = [ctypes.c_uint, vp]
+        L.td_timestep_table.argtypes = [vp, vp, i, i, vp, vp]
         L.td_lmhead_commit_static.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, vp, vp, vp,
                                                vp, vp, vp, vp]
         for name in EXPORTED:
@@ -181,9 +187,10 @@ def _paging(page_table, n_pages):
 
 
 def td_block_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len=None, o=None, lse=None,
-                       ws=None, stream=None, page_table=None, n_pages=0):
+                       ws=None, stream=None, page_table=None, n_pages=0,
+                       precision: int = TD_ATTN_P_BF16):
     """page_table [B, max_pages] int32 with k_ctx / v_ctx as page pools [n_pages, Hkv, 128, D]
-    selects the paged layout."""
+    selects the paged layout; precision: TD_ATTN_P_BF16 or TD_ATTN_P_SPLIT."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     if o is None:
         o = torch.empty_like(q)
@@ -192,7 +199,8 @@ def td_block_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len=None, o=None
     _check("td_block_attention",
            lib().td_block_attention(ctypes.byref(dm), _ptr(q), _ptr(k_blk), _ptr(v_blk),
                                     _ptr(k_ctx), _ptr(v_ctx), _ptr(ctx_len),
-                                    _byref_or_null(_paging(page_table, n_pages)), _ptr(o),
+                                    _byref_or_null(_paging(page_table, n_pages)),
+                                    int(precision), _ptr(o),
                                     _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
     return o
 
@@ -201,9 +209,10 @@ def _byref_or_null(x):
     return None if x is None else ctypes.byref(x)
 
 
-def _opts(rule, rope_theta, page_table, n_pages):
+def _opts(rule, rope_theta, page_table, n_pages, h_out=None, attn_precision=0):
     pg = _paging(page_table, n_pages)
-    return td_step_opts(int(rule), float(rope_theta), pg if pg is not None else td_paging())
+    return td_step_opts(int(rule), float(rope_theta), pg if pg is not None else td_paging(),
+                        _ptr(h_out), int(attn_precision))
 
 
 def _outs(B, S, device, conf, pred, n_committed, all_done):
@@ -263,9 +272,12 @@ def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tok
                     h=None, emb=None, pos=None, ctx_len=None, conf=None, pred=None,
                     n_committed=None, all_done=None, ws=None, stream=None,
                     rule: int = TD_COMMIT_CONFIDENCE, rope_theta: float = 0.0,
-                    page_table=None, n_pages: int = 0):
+                    page_table=None, n_pages: int = 0, h_out=None,
+                    attn_precision: int = TD_ATTN_P_BF16):
     """One denoising step; tokens / masked updated in place.
-    rule: commit rule; rope_theta > 0: rotary variant (see td_step_opts in include/td.h).
+    rule: commit rule; rope_theta > 0: rotary variant (see td_step_opts in include/td.h);
+    h_out (bf16 [B*S, d] device tensor): receives the hidden state after the last layer;
+    attn_precision: TD_ATTN_P_BF16 or TD_ATTN_P_SPLIT.
     Returns (conf, pred, n_committed, all_done)."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     dev = w_lm.device
@@ -277,7 +289,8 @@ def td_denoise_step(dims, layers, w_lm, phi_t, t: int, T: int, gamma: float, tok
     _check("td_denoise_step",
            lib().td_denoise_step(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(h), _ptr(emb),
                                  _ptr(pos), _ptr(w_lm), _ptr(phi_t), t, T, gamma,
-                                 ctypes.byref(_opts(rule, rope_theta, page_table, n_pages)),
+                                 ctypes.byref(_opts(rule, rope_theta, page_table, n_pages,
+                                                    h_out, attn_precision)),
                                  _ptr(tokens),
                                  _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
                                  _ptr(all_done), _ptr(ws), ws.numel(), _stream(stream)))
@@ -288,7 +301,8 @@ def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: floa
                     masked, t_start: int = 1, ctx_len=None, conf=None, pred=None,
                     n_committed=None, all_done=None, ws=None, stream=None,
                     rule: int = TD_COMMIT_CONFIDENCE, rope_theta: float = 0.0,
-                    page_table=None, n_pages: int = 0) -> int:
+                    page_table=None, n_pages: int = 0,
+                    attn_precision: int = TD_ATTN_P_BF16) -> int:
     """Runs the block decode loop in place on tokens / masked; returns the steps taken."""
     dm = dims if isinstance(dims, td_dims) else dims_from(dims)
     dev = w_lm.device
@@ -301,7 +315,8 @@ def td_decode_block(dims, layers, emb, pos, w_lm, phi_table, T: int, gamma: floa
     _check("td_decode_block",
            lib().td_decode_block(ctypes.byref(dm), arr, _ptr(ctx_len), _ptr(emb), _ptr(pos),
                                  _ptr(w_lm), _ptr(phi_table), t_start, T, gamma,
-                                 ctypes.byref(_opts(rule, rope_theta, page_table, n_pages)),
+                                 ctypes.byref(_opts(rule, rope_theta, page_table, n_pages,
+                                                    None, attn_precision)),
                                  _ptr(tokens),
                                  _ptr(masked), _ptr(conf), _ptr(pred), _ptr(n_committed),
                                  _ptr(all_done), ctypes.byref(steps), _ptr(ws), ws.numel(),
@@ -328,3 +343,14 @@ def td_check_bounded_wait(limit_us: int, stream=None) -> None:
     """Launches the bounded-wait diagnostic (see include/td.h); read the result with
     td_device_error()."""
     _check("td_check_bounded_wait", lib().td_check_bounded_wait(int(limit_us), _stream(stream)))
+
+
+def td_timestep_table(w_t, b_t, T: int, phi_table=None, stream=None) -> torch.Tensor:
+    """The adaLN-single table phi(t), t = 1..T, fp32 [T, 6, d], from W_t fp32 [6d, 256] and
+    b_t fp32 [6d] (see include/td.h); allocated when not given."""
+    d = int(b_t.numel()) // 6
+    if phi_table is None:
+        phi_table = torch.empty((T, 6, d), dtype=torch.float32, device=b_t.device)
+    _check("td_timestep_table", lib().td_timestep_table(_ptr(w_t), _ptr(b_t), d, int(T),
+                                                        _ptr(phi_table), _stream(stream)))
+    return phi_table

@@ -193,7 +193,10 @@ __device__ __forceinline__ void cursor_next(TileCursor& c, const AttnParams& p, 
   cursor_next_segment(c, p, lo, hi, u_last);
 }
 
-template <int D, bool kPaged>
+// kSplitP: P enters O += P V as two bf16 values (hi = bf16(P) at TMEM columns 256.., lo =
+// bf16(P - hi) at 320..) with a second product per key step; P is then single buffered
+// (softmax of tile n waits for the P V of tile n - 1).
+template <int D, bool kPaged, bool kSplitP>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fused_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmKc,
@@ -368,11 +371,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!mbar_wait(&v_full[st], (n / kVSlots) & 1, ERR_WAIT_TMA)) break;
         tc_fence_after();
         const uint64_t vdesc = sdesc_sw128(smem_u32(sV + st * L::kKBytes), L::kKVHalf, 1024);
-        const uint32_t pa = tmem + 256 + buf * 64;
+        const uint32_t pa = tmem + 256 + (kSplitP ? 0 : buf * 64);
 #pragma unroll
         for (int kk = 0; kk < kKeyTile / 16; ++kk)
           mma_bf16_ts(tmem, pa + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_pv,
                       !(first && kk == 0));
+        if constexpr (kSplitP) {
+#pragma unroll
+          for (int kk = 0; kk < kKeyTile / 16; ++kk)
+            mma_bf16_ts(tmem, pa + 64 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_pv, 1);
+        }
         mma_commit(&o_done[buf]);
         mma_commit(&v_empty[st]);
         cursor_next(c, p, lo, hi, u_last);
@@ -497,8 +505,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tmem_st32(tmem + lane_off + kh * DH + 32 * k, o);
           }
         }
-        // P[buf] was last read by the PV of tile n-2
-        if (n >= 2) mbar_wait(&o_done[buf], ((n - 2) >> 1) & 1, ERR_WAIT_MMA);
+        // P[buf] was last read by the PV of tile n-2 (split P: the one P area by tile n-1)
+        if constexpr (kSplitP) {
+          if (n >= 1) mbar_wait(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, ERR_WAIT_MMA);
+        } else {
+          if (n >= 2) mbar_wait(&o_done[buf], ((n - 2) >> 1) & 1, ERR_WAIT_MMA);
+        }
         tc_fence_after();
         // P = 2^(x*scale - m) rounded to bf16, two per TMEM column (keys 64kh.. -> columns
         // 32kh.. of P[buf]); the running sum adds the fp32 values
@@ -506,15 +518,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          uint32_t pk[16];
+          uint32_t pk[16], pl[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float e0 = ex2_approx(fmaf(x[32 * k + 2 * j], sc, mneg));
             const float e1 = ex2_approx(fmaf(x[32 * k + 2 * j + 1], sc, mneg));
             pk[j] = pack_bf16x2(e0, e1);
+            if constexpr (kSplitP)
+              pl[j] = pack_bf16x2(e0 - bf16lo_to_f32(pk[j]), e1 - bf16hi_to_f32(pk[j]));
             ls[j & 3] += e0 + e1;
           }
-          tmem_st16(tmem + lane_off + 256 + buf * 64 + kh * 32 + 16 * k, pk);
+          const uint32_t pcol = 256 + (kSplitP ? 0 : buf * 64) + kh * 32 + 16 * k;
+          tmem_st16(tmem + lane_off + pcol, pk);
+          if constexpr (kSplitP) tmem_st16(tmem + lane_off + pcol + 64, pl);
         }
         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_st_wait();

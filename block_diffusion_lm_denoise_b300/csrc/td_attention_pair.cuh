@@ -56,7 +56,11 @@ struct PairSmem {
   static constexpr int kBytes = kOffBar + 512 + 1024;
 };
 
-template <bool kPaged>
+// kSplitP: P enters O += P V as two bf16 values, hi = bf16(P) over the first 64 columns of
+// SP[buf] and lo = bf16(P - hi) over the other 64 (both warps of a lane quarter have read
+// their scores by then), with a second product per key step: P is then carried to about
+// 2^-17 relative instead of 2^-9.
+template <bool kPaged, bool kSplitP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmKc,
@@ -285,9 +289,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
         // one 64-column swizzle atom of V per CTA: the leading byte offset is not used
         const uint64_t vdesc = sdesc_sw128(smem_u32(sV + st * L::kVBytes), L::kVBytes, 1024);
         const uint32_t pa = tmem + 128 + 128 * buf;
-        for (int kk = 0; kk < nk; ++kk)
-          mma_pair_ts(tmem, pa + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_pv,
-                      !(first && kk == 0));
+        // a full tile's eight products go out as straight-line code: a branch between two
+        // tcgen05.mma instructions costs the issuing thread about 100 cycles, more than the
+        // 64 the tensor pipe needs for one product
+        if (nk == kKeyTile / 16) {
+#pragma unroll
+          for (int kk = 0; kk < kKeyTile / 16; ++kk)
+            mma_pair_ts(tmem, pa + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_pv,
+                        !(first && kk == 0));
+          if constexpr (kSplitP) {
+#pragma unroll
+            for (int kk = 0; kk < kKeyTile / 16; ++kk)
+              mma_pair_ts(tmem, pa + 64 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_pv, 1);
+          }
+        } else {
+          for (int kk = 0; kk < nk; ++kk)
+            mma_pair_ts(tmem, pa + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_pv,
+                        !(first && kk == 0));
+          if constexpr (kSplitP)
+            for (int kk = 0; kk < nk; ++kk)
+              mma_pair_ts(tmem, pa + 64 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_pv, 1);
+        }
         mma_commit_pair(&o_done[buf], 3);
         mma_commit_pair(&v_empty[st], 3);
         cursor_next(c, p, lo, hi, u_last);
@@ -404,15 +426,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          uint32_t pk[16];
+          uint32_t pk[16], pl[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float e0 = ex2_approx(fmaf(x[32 * k + 2 * j], sc, mneg));
             const float e1 = ex2_approx(fmaf(x[32 * k + 2 * j + 1], sc, mneg));
             pk[j] = pack_bf16x2(e0, e1);
+            if constexpr (kSplitP)
+              pl[j] = pack_bf16x2(e0 - bf16lo_to_f32(pk[j]), e1 - bf16hi_to_f32(pk[j]));
             ls[j & 3] += e0 + e1;
           }
           tmem_st16(sp + kh * 32 + 16 * k, pk);
+          if constexpr (kSplitP) tmem_st16(sp + 64 + kh * 32 + 16 * k, pl);
         }
         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_st_wait();

@@ -183,7 +183,13 @@ AttnPlan plan_attention(const td_dims* dm, int nsm) {
   a.ncta = a.n_teams * team_ctas;
   const long long tiles = (a.total + a.n_teams - 1) / a.n_teams;
   a.max_seg = (int)((tiles + a.T - 1) / a.T) + 1;
-  const size_t recs = (size_t)a.n_teams * a.NC * a.max_seg;
+  // partial records: sized for the largest plan any problem up to this one can take (every
+  // possible team splitting its range), so that the workspace never shrinks as B grows and a
+  // buffer sized for one batch serves every smaller one
+  const long long tiles_bound = (a.total + max_teams - 1) / max_teams;
+  const size_t recs_bound =
+      (size_t)max_teams * a.NC * (size_t)(((tiles_bound + a.T - 1) / a.T) + 1);
+  const size_t recs = std::max((size_t)a.n_teams * a.NC * a.max_seg, recs_bound);
   a.part_o_bytes = align_up(recs * a.R * dm->D * sizeof(float));
   a.part_ml_bytes = align_up(recs * a.R * 2 * sizeof(float));
   return a;
@@ -295,10 +301,35 @@ td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, 
   return TD_OK;
 }
 
+// One instantiation of the attention kernels per (layout, P precision).
+template <bool kPaged, bool kSplit>
+cudaError_t launch_attn_kernel(const AttnPlan& a, int D, const CUtensorMap& mq,
+                               const CUtensorMap& mkc, const CUtensorMap& mvc,
+                               const CUtensorMap& mkb, const CUtensorMap& mvb,
+                               const AttnParams& p, cudaStream_t st) {
+  if (a.pair) {
+    auto k = attn_pair_kernel<kPaged, kSplit>;
+    cudaError_t e = set_smem(k, PairSmem::kBytes);
+    if (e != cudaSuccess) return e;
+    k<<<a.ncta, kAttnThreads, PairSmem::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
+  } else if (D == 128) {
+    auto k = attn_fused_kernel<128, kPaged, kSplit>;
+    cudaError_t e = set_smem(k, AttnSmem<128>::kBytes);
+    if (e != cudaSuccess) return e;
+    k<<<a.ncta, kAttnThreads, AttnSmem<128>::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
+  } else {
+    auto k = attn_fused_kernel<64, kPaged, kSplit>;
+    cudaError_t e = set_smem(k, AttnSmem<64>::kBytes);
+    if (e != cudaSuccess) return e;
+    k<<<a.ncta, kAttnThreads, AttnSmem<64>::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
+  }
+  return cudaGetLastError();
+}
+
 td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, const void* v_blk,
                         const void* k_ctx, const void* v_ctx, const int* ctx_len,
-                        const td_paging* pg, void* o, float* lse, void* ws, cudaStream_t st,
-                        int nsm, const int* skip = nullptr) {
+                        const td_paging* pg, int precision, void* o, float* lse, void* ws,
+                        cudaStream_t st, int nsm, const int* skip = nullptr) {
   const bool paged = pg != nullptr && pg->page_table != nullptr;
   const AttnPlan a = plan_attention(dm, nsm);
   const int D = dm->D;
@@ -312,7 +343,7 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
   }
   // K/V boxes: the single-SM kernel loads whole 128-key tiles (block keys: S rows); the pair
   // kernel loads its half: 64 keys of K, 64 head dims of V (block keys: 64 / 128 rows, the
-  // rows beyond S arrive as zeros)
+  // rows beyond S lie outside the tensor and arrive as zeros)
   const uint32_t kb_rows = a.pair ? 64 : kKeyTile, vb_rows = kKeyTile;
   const uint32_t blk_k = a.pair ? 64 : (uint32_t)dm->S, blk_v = a.pair ? 128 : (uint32_t)dm->S;
   {
@@ -357,20 +388,15 @@ td_status run_attention(const td_dims* dm, const void* q, const void* k_blk, con
   p.out = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  if (a.pair) {
-    auto k = paged ? attn_pair_kernel<true> : attn_pair_kernel<false>;
-    TD_CUDA(set_smem(k, PairSmem::kBytes));
-    k<<<a.ncta, kAttnThreads, PairSmem::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
-  } else if (D == 128) {
-    auto k = paged ? attn_fused_kernel<128, true> : attn_fused_kernel<128, false>;
-    TD_CUDA(set_smem(k, AttnSmem<128>::kBytes));
-    k<<<a.ncta, kAttnThreads, AttnSmem<128>::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
-  } else {
-    auto k = paged ? attn_fused_kernel<64, true> : attn_fused_kernel<64, false>;
-    TD_CUDA(set_smem(k, AttnSmem<64>::kBytes));
-    k<<<a.ncta, kAttnThreads, AttnSmem<64>::kBytes, st>>>(mq, mkc, mvc, mkb, mvb, p);
-  }
-  TD_CUDA(cudaGetLastError());
+  const bool split = precision == TD_ATTN_P_SPLIT;
+  cudaError_t ke;
+  if (paged)
+    ke = split ? launch_attn_kernel<true, true>(a, D, mq, mkc, mvc, mkb, mvb, p, st)
+               : launch_attn_kernel<true, false>(a, D, mq, mkc, mvc, mkb, mvb, p, st);
+  else
+    ke = split ? launch_attn_kernel<false, true>(a, D, mq, mkc, mvc, mkb, mvb, p, st)
+               : launch_attn_kernel<false, false>(a, D, mq, mkc, mvc, mkb, mvb, p, st);
+  TD_CUDA(ke);
   if (a.split) {
     const dim3 grid(a.n_units * a.NC, (a.R + kMergeRows - 1) / kMergeRows);
     attn_merge_kernel<<<grid, kMergeRows * (D / 4), 0, st>>>(p);
@@ -437,9 +463,10 @@ StepWs carve_step(const td_dims* dm, void* base, int nsm) {
 td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len, const void* h,
                    const void* emb, const void* pos, const void* w_lm, const float* phi_t,
                    int t, int T, float gamma, int rule, float rope_theta,
-                   const td_paging* paging, int* tokens, unsigned char* masked, float* conf,
-                   int* pred, int* n_committed, int* all_done, void* ws, cudaStream_t st,
-                   int nsm, const int* skip = nullptr, int* steps = nullptr) {
+                   const td_paging* paging, int precision, int* tokens, unsigned char* masked,
+                   float* conf, int* pred, int* n_committed, int* all_done, void* ws,
+                   cudaStream_t st, int nsm, const int* skip = nullptr, int* steps = nullptr,
+                   void* h_out = nullptr) {
   const StepWs w = carve_step(dm, ws, nsm);
   const int M = dm->B * dm->S;
   const int d = dm->d;
@@ -478,19 +505,24 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
             ? gemm_dispatch<EPI_QKV_ROPE>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn)
             : gemm_dispatch<EPI_QKV>(w.xmod, L.wqkv, M, nq + 2 * nk, d, g1, st, nsm, bn);
     if (s != TD_OK) return s;
-    s = run_attention(dm, w.q, w.k, w.v, L.k_ctx, L.v_ctx, ctx_len, paging, w.o, nullptr, w.attn,
-                      st, nsm, skip);
+    s = run_attention(dm, w.q, w.k, w.v, L.k_ctx, L.v_ctx, ctx_len, paging, precision, w.o,
+                      nullptr, w.attn, st, nsm, skip);
     if (s != TD_OK) return s;
     GemmParams g2{};
     g2.h = w.h; g2.gate = w.gate; g2.skip = skip;
-    if (l == dm->n_layers - 1) {
+    if (l == dm->n_layers - 1 && h_out == nullptr) {
+      // the last layer writes only the rows the LM head evaluates, compacted
       g2.row_pos = w.row_pos;
       g2.h_out = w.h_lm;
     }
     s = gemm_dispatch<EPI_RESID>(w.o, L.wo, M, d, nq, g2, st, nsm, bn);
     if (s != TD_OK) return s;
   }
-  if (dm->n_layers == 0) {
+  if (dm->n_layers == 0 || h_out != nullptr) {
+    // every row of the final hidden state is in w.h: report it if asked, then gather the
+    // rows the LM head evaluates (the same values the compacted epilogue writes)
+    if (h_out != nullptr)
+      TD_CUDA(cudaMemcpyAsync(h_out, w.h, (size_t)M * d * 2, cudaMemcpyDeviceToDevice, st));
     gather_rows_kernel<<<M, 256, 0, st>>>(w.h, w.row_pos, w.h_lm, d, skip);
     TD_CUDA(cudaGetLastError());
   }
@@ -528,12 +560,18 @@ void set_all_smem() {
   set_smem(gemm_tn_kernel<256, 4, EPI_LMHEAD>, GemmSmem<256, 4>::kBytes);
   set_smem(gemm_tn_kernel<128, 6, EPI_QKV_ROPE>, GemmSmem<128, 6>::kBytes);
   set_smem(gemm_tn_kernel<256, 4, EPI_QKV_ROPE>, GemmSmem<256, 4>::kBytes);
-  set_smem(attn_fused_kernel<128, false>, AttnSmem<128>::kBytes);
-  set_smem(attn_fused_kernel<64, false>, AttnSmem<64>::kBytes);
-  set_smem(attn_pair_kernel<false>, PairSmem::kBytes);
-  set_smem(attn_fused_kernel<128, true>, AttnSmem<128>::kBytes);
-  set_smem(attn_fused_kernel<64, true>, AttnSmem<64>::kBytes);
-  set_smem(attn_pair_kernel<true>, PairSmem::kBytes);
+  set_smem(attn_fused_kernel<128, false, false>, AttnSmem<128>::kBytes);
+  set_smem(attn_fused_kernel<64, false, false>, AttnSmem<64>::kBytes);
+  set_smem(attn_pair_kernel<false, false>, PairSmem::kBytes);
+  set_smem(attn_fused_kernel<128, true, false>, AttnSmem<128>::kBytes);
+  set_smem(attn_fused_kernel<64, true, false>, AttnSmem<64>::kBytes);
+  set_smem(attn_pair_kernel<true, false>, PairSmem::kBytes);
+  set_smem(attn_fused_kernel<128, false, true>, AttnSmem<128>::kBytes);
+  set_smem(attn_fused_kernel<64, false, true>, AttnSmem<64>::kBytes);
+  set_smem(attn_pair_kernel<false, true>, PairSmem::kBytes);
+  set_smem(attn_fused_kernel<128, true, true>, AttnSmem<128>::kBytes);
+  set_smem(attn_fused_kernel<64, true, true>, AttnSmem<64>::kBytes);
+  set_smem(attn_pair_kernel<true, true>, PairSmem::kBytes);
 }
 
 struct LoopKey {
@@ -565,7 +603,7 @@ cudaStream_t capture_stream() {
 td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx_len,
                        const void* emb, const void* pos, const void* w_lm,
                        const float* phi_table, int t_start, int T, float gamma, int rule,
-                       float rope_theta, const td_paging* paging, int* tokens,
+                       float rope_theta, const td_paging* paging, int precision, int* tokens,
                        unsigned char* masked, float* conf, int* pred,
                        int* n_committed, int* all_done, void* ws, size_t ws_bytes,
                        cudaStream_t st, int nsm, int* steps_taken, int* done) {
@@ -585,6 +623,7 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
   std::memcpy(&rbits, &rope_theta, 4);
   key.v.push_back(rbits);
   u(paging ? paging->page_table : nullptr);
+  key.v.push_back((uint64_t)precision);
   key.v.push_back(paging ? (uint64_t)paging->max_pages : 0);
   key.v.push_back(paging ? (uint64_t)paging->n_pages : 0);
   for (int l = 0; l < dm->n_layers; ++l) {
@@ -616,8 +655,8 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
       for (int t = t_start; t <= T && s == TD_OK; ++t)
         s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
                      phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, rope_theta,
-                     paging, tokens, masked, conf, pred, n_committed, all_done, ws, cs, nsm,
-                     all_done, w.loop);
+                     paging, precision, tokens, masked, conf, pred, n_committed, all_done, ws,
+                     cs, nsm, all_done, w.loop);
       cudaGraph_t g = nullptr;
       const cudaError_t ee = cudaStreamEndCapture(cs, &g);
       if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
@@ -668,13 +707,20 @@ bool paging_ok(const td_dims* dm, const td_paging* pg) {
 
 // Options of a step (NULL: confidence masking, no rotation, contiguous caches); false if
 // they are invalid.
+bool precision_ok(int precision) {
+  return precision == TD_ATTN_P_BF16 || precision == TD_ATTN_P_SPLIT;
+}
+
 bool read_opts(const td_dims* dm, const td_step_opts* opts, int* rule, float* rope_theta,
-               const td_paging** paging) {
+               const td_paging** paging, void** h_out, int* precision) {
   *rule = opts ? opts->rule : TD_COMMIT_CONFIDENCE;
   *rope_theta = opts ? opts->rope_theta : 0.f;
   *paging = (opts && opts->paging.page_table) ? &opts->paging : nullptr;
+  *h_out = opts ? opts->h_out : nullptr;
+  *precision = opts ? opts->attn_precision : TD_ATTN_P_BF16;
   return rule_ok(*rule) && std::isfinite(*rope_theta) && *rope_theta >= 0.f &&
-         paging_ok(dm, *paging);
+         paging_ok(dm, *paging) && (*h_out == nullptr || aligned16(*h_out)) &&
+         precision_ok(*precision);
 }
 
 bool ws_ok(const void* ws, size_t have, size_t need) {
@@ -732,11 +778,11 @@ td_status td_adaln_modulate(const void* h, const float* E, const float* phi, int
 
 td_status td_block_attention(const td_dims* dims, const void* q, const void* k_blk,
                              const void* v_blk, const void* k_ctx, const void* v_ctx,
-                             const int* ctx_len, const td_paging* paging, void* o, float* lse,
-                             void* ws, size_t ws_bytes, void* stream) {
+                             const int* ctx_len, const td_paging* paging, int precision,
+                             void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
   td_status s = check_dims(dims, false);
   if (s != TD_OK) return s;
-  if (!paging_ok(dims, paging)) return TD_ERR_INVALID_ARG;
+  if (!paging_ok(dims, paging) || !precision_ok(precision)) return TD_ERR_INVALID_ARG;
   if (!q || !k_blk || !v_blk || !o) return TD_ERR_INVALID_ARG;
   if (dims->Lmax > 0 && (!k_ctx || !v_ctx)) return TD_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_blk) || !aligned16(v_blk) || !aligned16(o) ||
@@ -744,8 +790,8 @@ td_status td_block_attention(const td_dims* dims, const void* q, const void* k_b
     return TD_ERR_INVALID_ARG;
   const int nsm = sm_count();
   if (!ws_ok(ws, ws_bytes, attn_ws_bytes(dims, nsm))) return TD_ERR_WORKSPACE;
-  return run_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, paging, o, lse, ws,
-                       (cudaStream_t)stream, nsm);
+  return run_attention(dims, q, k_blk, v_blk, k_ctx, v_ctx, ctx_len, paging, precision, o, lse,
+                       ws, (cudaStream_t)stream, nsm);
 }
 
 td_status td_lmhead_commit(const td_dims* dims, const void* h, const void* w_lm, float gamma,
@@ -775,7 +821,10 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
   int rule = 0;
   float rope_theta = 0.f;
   const td_paging* paging = nullptr;
-  if (!read_opts(dims, opts, &rule, &rope_theta, &paging)) return TD_ERR_INVALID_ARG;
+  void* h_out = nullptr;
+  int precision = 0;
+  if (!read_opts(dims, opts, &rule, &rope_theta, &paging, &h_out, &precision))
+    return TD_ERR_INVALID_ARG;
   if ((s = check_layers(dims, layers)) != TD_OK) return s;
   if (!w_lm || !phi_t || !tokens || !masked || !conf || !pred || !n_committed || !all_done)
     return TD_ERR_INVALID_ARG;
@@ -787,8 +836,9 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
   const int nsm = sm_count();
   if (!ws_ok(ws, ws_bytes, carve_step(dims, nullptr, nsm).total)) return TD_ERR_WORKSPACE;
   return run_step(dims, layers, ctx_len, h, emb, pos, w_lm, phi_t, t, T, gamma, rule,
-                  rope_theta, paging, tokens, masked,
-                  conf, pred, n_committed, all_done, ws, (cudaStream_t)stream, nsm);
+                  rope_theta, paging, precision, tokens, masked,
+                  conf, pred, n_committed, all_done, ws, (cudaStream_t)stream, nsm, nullptr,
+                  nullptr, h_out);
 }
 
 td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int* ctx_len,
@@ -802,7 +852,11 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   int rule = 0;
   float rope_theta = 0.f;
   const td_paging* paging = nullptr;
-  if (!read_opts(dims, opts, &rule, &rope_theta, &paging)) return TD_ERR_INVALID_ARG;
+  void* h_out = nullptr;
+  int precision = 0;
+  if (!read_opts(dims, opts, &rule, &rope_theta, &paging, &h_out, &precision))
+    return TD_ERR_INVALID_ARG;
+  if (h_out != nullptr) return TD_ERR_INVALID_ARG;   // a loop has no single final state
   if ((s = check_layers(dims, layers)) != TD_OK) return s;
   if (!emb || !pos || !w_lm || !phi_table || !tokens || !masked || !conf || !pred ||
       !n_committed || !all_done || !steps_taken)
@@ -825,8 +879,8 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   int done = 0;
   if (t_start <= T) {
     s = decode_graph(dims, layers, ctx_len, emb, pos, w_lm, phi_table, t_start, T, gamma, rule,
-                     rope_theta, paging, tokens, masked, conf, pred, n_committed, all_done, ws, ws_bytes, st, nsm,
-                     steps_taken, &done);
+                     rope_theta, paging, precision, tokens, masked, conf, pred, n_committed,
+                     all_done, ws, ws_bytes, st, nsm, steps_taken, &done);
     if (s == TD_OK) return done ? TD_OK : TD_ERR_NOT_CONVERGED;
     if (s != TD_ERR_UNSUPPORTED) return s;
   }
@@ -835,7 +889,8 @@ td_status td_decode_block(const td_dims* dims, const td_layer* layers, const int
   for (int t = t_start; t <= T; ++t) {
     s = run_step(dims, layers, ctx_len, nullptr, emb, pos, w_lm,
                  phi_table + (size_t)(t - 1) * 6 * dims->d, t, T, gamma, rule, rope_theta,
-                 paging, tokens, masked, conf, pred, n_committed, all_done, ws, st, nsm);
+                 paging, precision, tokens, masked, conf, pred, n_committed, all_done, ws, st,
+                 nsm);
     if (s != TD_OK) return s;
     TD_CUDA(cudaMemcpyAsync(&done, all_done, sizeof(int), cudaMemcpyDeviceToHost, st));
     TD_CUDA(cudaStreamSynchronize(st));
@@ -875,8 +930,20 @@ td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv*
         paged ? paging->max_pages : 0, paged ? paging->n_pages : 0);
     TD_CUDA(cudaGetLastError());
   }
-  kv_len_update_kernel<<<(dims->B + 255) / 256, 256, 0, st>>>(ctx_len, dims->B, dims->S,
-                                                              dims->Lmax);
+  kv_len_update_kernel<<<(dims->B + 255) / 256, 256, 0, st>>>(
+      ctx_len, dims->B, dims->S, dims->Lmax, paged ? paging->page_table : nullptr,
+      paged ? paging->max_pages : 0, paged ? paging->n_pages : 0);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
+}
+
+td_status td_timestep_table(const float* w_t, const float* b_t, int d, int T, float* phi_table,
+                            void* stream) {
+  if (!w_t || !b_t || !phi_table || d <= 0 || T <= 0 || T > 65536) return TD_ERR_INVALID_ARG;
+  if ((long long)6 * d > (1ll << 30)) return TD_ERR_UNSUPPORTED;
+  const int rows = 6 * d;
+  timestep_table_kernel<<<(rows + kTsWarps - 1) / kTsWarps, 32 * kTsWarps, 0,
+                          (cudaStream_t)stream>>>(w_t, b_t, rows, T, phi_table);
   TD_CUDA(cudaGetLastError());
   return TD_OK;
 }
@@ -919,7 +986,8 @@ static __device__ __align__(256) unsigned char g_lm_static_scratch[kStaticScratc
 std::mutex g_static_mu;
 void* g_static_addr[kMaxDevices] = {};
 
-// Device address of the scratch on the current device, looked up once per device.
+// Device address of the scratch on the current device, looked up once per device and kept
+// for the life of the process (stale after a cudaDeviceReset() of that device).
 td_status static_scratch_addr(void** out) {
   int dev = -1;
   TD_CUDA(cudaGetDevice(&dev));

@@ -479,6 +479,52 @@ __global__ void rope_table_kernel(const int* __restrict__ ctx_len, int B, int S,
   }
 }
 
+// adaLN-single timestep map: phi(t) = W_t e(t / T) + b_t for t = 1..T, e the 256-wide
+// sinusoidal embedding of s = 1000 t / T (e[j] = cos(s w_j), e[128 + j] = sin(s w_j),
+// w_j = 10000^(-j / 128)). One warp per output row k of W_t [6d, 256] (its 256 weights, eight
+// a lane, read once) for a chunk of up to kTsChunk steps; the embeddings of the chunk are
+// built in shared memory, everything in double precision, the result rounded to float once.
+constexpr int kTsDim = 256;
+constexpr int kTsChunk = 16;
+constexpr int kTsWarps = 8;
+
+__global__ void __launch_bounds__(32 * kTsWarps)
+    timestep_table_kernel(const float* __restrict__ w_t, const float* __restrict__ b_t,
+                          int rows, int T, float* __restrict__ phi) {
+  __shared__ double emb[kTsChunk][kTsDim];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = blockIdx.x * kTsWarps + warp;
+  double w[kTsDim / 32];
+  if (k < rows) {
+#pragma unroll
+    for (int i = 0; i < kTsDim / 32; ++i) w[i] = (double)__ldg(&w_t[(size_t)k * kTsDim + lane + 32 * i]);
+  }
+  const double bias = k < rows ? (double)__ldg(&b_t[k]) : 0.0;
+  for (int t0 = 0; t0 < T; t0 += kTsChunk) {
+    const int nt = min(kTsChunk, T - t0);
+    __syncthreads();
+    for (int x = threadIdx.x; x < nt * (kTsDim / 2); x += blockDim.x) {
+      const int tt = x / (kTsDim / 2), j = x % (kTsDim / 2);
+      const double s = 1000.0 * (double)(t0 + tt + 1) / (double)T;
+      const double a = s * pow(10000.0, -(double)j / (double)(kTsDim / 2));
+      double sn, cn;
+      sincos(a, &sn, &cn);
+      emb[tt][j] = cn;
+      emb[tt][kTsDim / 2 + j] = sn;
+    }
+    __syncthreads();
+    if (k >= rows) continue;
+    for (int tt = 0; tt < nt; ++tt) {
+      double acc = 0.0;
+#pragma unroll
+      for (int i = 0; i < kTsDim / 32; ++i) acc = fma(w[i], emb[tt][lane + 32 * i], acc);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) phi[(size_t)(t0 + tt) * rows + k] = (float)(acc + bias);
+    }
+  }
+}
+
 // One thread waits, through the same bounded wait every kernel uses, on a barrier that
 // nothing completes: the wait must give up after limit_ns and record ERR_WAIT_EPI.
 __global__ void wait_check_kernel(unsigned long long limit_ns) {
@@ -494,7 +540,19 @@ __global__ void wait_check_kernel(unsigned long long limit_ns) {
 // per 16-byte chunk; sequences whose cache would pass Lmax are skipped (flagged by the
 // length update below).
 // With page_table set, the caches are pools [n_pages][Hkv][128][D] and position pos of
-// sequence b lives in page page_table[b * max_pages + pos / 128], row pos % 128.
+// sequence b lives in page page_table[b * max_pages + pos / 128], row pos % 128. A sequence
+// any of whose new positions maps to an entry outside [0, n_pages) is skipped whole (the
+// length update flags it and keeps its length).
+
+// True if every page-table entry of positions L .. L + S - 1 of sequence b is in range
+// (S <= 64 < 128: the positions span at most two pages).
+__device__ __forceinline__ bool append_pages_ok(const int* page_table, int max_pages,
+                                                int n_pages, int b, int L, int S) {
+  const int p0 = page_table[(size_t)b * max_pages + L / 128];
+  const int p1 = page_table[(size_t)b * max_pages + (L + S - 1) / 128];
+  return p0 >= 0 && p0 < n_pages && p1 >= 0 && p1 < n_pages;
+}
+
 __global__ void kv_append_kernel(const uint16_t* __restrict__ k_new,
                                  const uint16_t* __restrict__ v_new, uint16_t* __restrict__ k_ctx,
                                  uint16_t* __restrict__ v_ctx, const int* __restrict__ ctx_len,
@@ -511,14 +569,12 @@ __global__ void kv_append_kernel(const uint16_t* __restrict__ k_new,
     const int b = (int)(row / ((long long)Hkv * S));
     const int L = ctx_len[b];
     if (L < 0 || L + S > Lmax) continue;
+    if (page_table != nullptr && !append_pages_ok(page_table, max_pages, n_pages, b, L, S))
+      continue;
     const int pos = L + i;
     size_t dst;
     if (page_table != nullptr) {
       const int page = page_table[(size_t)b * max_pages + pos / 128];
-      if (page < 0 || page >= n_pages) {
-        record_error(ERR_BAD_PAGE);
-        continue;
-      }
       dst = (((size_t)page * Hkv + g) * 128 + (size_t)(pos % 128)) * D + (size_t)c * 8;
     } else {
       dst = (((size_t)b * Hkv + g) * Lmax + (size_t)pos) * D + (size_t)c * 8;
@@ -529,12 +585,17 @@ __global__ void kv_append_kernel(const uint16_t* __restrict__ k_new,
   }
 }
 
-// After every layer's append: ctx_len[b] += S, or the overflow is recorded.
-__global__ void kv_len_update_kernel(int* ctx_len, int B, int S, int Lmax) {
+// After every layer's append: ctx_len[b] += S, or the overflow (or, paged, an out-of-range
+// page entry of the new positions) is recorded and the length kept.
+__global__ void kv_len_update_kernel(int* ctx_len, int B, int S, int Lmax,
+                                     const int* __restrict__ page_table, int max_pages,
+                                     int n_pages) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int L = ctx_len[b];
   if (L < 0 || L + S > Lmax) record_error(ERR_CTX_FULL);
+  else if (page_table != nullptr && !append_pages_ok(page_table, max_pages, n_pages, b, L, S))
+    record_error(ERR_BAD_PAGE);
   else ctx_len[b] = L + S;
 }
 

@@ -114,8 +114,22 @@ typedef struct td_paging {
   int n_pages;
 } td_paging;
 
+/* Precision of the softmax probabilities P in the attention's O += P V product (the pages fix
+ * no arithmetic beyond BF16; this is a property of this library):
+ *   TD_ATTN_P_BF16   P is rounded to bf16 (about 2^-9 relative) for the product: the fast
+ *                    default.
+ *   TD_ATTN_P_SPLIT  P enters as the sum of two bf16 values, hi = bf16(P) and
+ *                    lo = bf16(P - hi) (P carried to about 2^-17 relative), at the cost of a
+ *                    second P V product per key tile. Stacked layers then follow an exact
+ *                    softmax more closely.
+ * Either way the products accumulate in fp32 and the output is rounded to bf16 once. */
+typedef enum td_attn_precision {
+  TD_ATTN_P_BF16 = 0,
+  TD_ATTN_P_SPLIT = 1
+} td_attn_precision;
+
 /* Options of a denoise step (td_denoise_step, td_decode_block); NULL means
- * { TD_COMMIT_CONFIDENCE, 0, no paging }.
+ * { TD_COMMIT_CONFIDENCE, 0, no paging, NULL, TD_ATTN_P_BF16 }.
  *   rule        a td_commit_rule.
  *   rope_theta  0: no positional rotation (the pages describe none; the embedding path adds
  *               the caller's position table instead). > 0: rotary variant, a reading of a
@@ -124,11 +138,20 @@ typedef struct td_paging {
  *               rounding, interleaved pairs (2j, 2j+1) of each head turned by
  *               pos * rope_theta^(-2j/D); the cached context keys are taken as already rotated
  *               by the context tower. Negative or non-finite: TD_ERR_INVALID_ARG.
- *   paging      the context caches' layout (td_paging; page_table NULL: contiguous). */
+ *   paging      the context caches' layout (td_paging; page_table NULL: contiguous).
+ *   h_out       NULL, or a device buffer, bf16 [B*S, d], 16-byte aligned, that receives the
+ *               block's hidden state after the last layer: every row, the LM head's input
+ *               (rows the step does not evaluate included). td_denoise_step only: a non-NULL
+ *               h_out given to td_decode_block returns TD_ERR_INVALID_ARG (a loop has no
+ *               single final state). Writing it changes no other output.
+ *   attn_precision  a td_attn_precision for every attention of the step (anything else:
+ *               TD_ERR_INVALID_ARG). */
 typedef struct td_step_opts {
   int rule;
   float rope_theta;
   td_paging paging;
+  void* h_out;
+  int attn_precision;
 } td_step_opts;
 
 /* Selector for td_workspace_size(). */
@@ -174,14 +197,15 @@ td_status td_adaln_modulate(const void* h, const float* E, const float* phi, int
  *   ctx_len int32 [B] or NULL (0 <= ctx_len[b] <= Lmax)
  *   paging  NULL (k_ctx, v_ctx contiguous as above) or a paged layout (td_paging: k_ctx,
  *           v_ctx are page pools)
+ *   precision  a td_attn_precision (anything else: TD_ERR_INVALID_ARG)
  *   o      bf16 [B, S, Hq, D] (written)
  *   lse    fp32 [B, S, Hq] or NULL: natural log of sum_j exp(q . keys_j / sqrt(D))
  *   ws     >= td_workspace_size(dims, TD_FN_BLOCK_ATTENTION) bytes.
  * Only B, S, Hq, Hkv, D, Lmax of dims are read. */
 td_status td_block_attention(const td_dims* dims, const void* q, const void* k_blk,
                              const void* v_blk, const void* k_ctx, const void* v_ctx,
-                             const int* ctx_len, const td_paging* paging, void* o, float* lse,
-                             void* ws, size_t ws_bytes, void* stream);
+                             const int* ctx_len, const td_paging* paging, int precision,
+                             void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /* LM head + confidence-masking commit ([chathome] generation and evaluation paragraphs:
  * tokens of the block commit when their confidence clears gamma; several commit per step).
@@ -271,12 +295,28 @@ typedef struct td_kv {
  * and the device error word reads ERR_CTX_FULL (0x600, see td_device_error).
  * With paging (non-NULL, page_table set) the caches are page pools and position pos of
  * sequence b is written to row pos % 128 of page page_table[b * max_pages + pos / 128]; the
- * caller maps the pages of the new positions before the call.
+ * caller maps the pages of the new positions before the call. A sequence whose new
+ * positions map to a page-table entry outside [0, n_pages) is left unchanged as well (no row
+ * written, ctx_len kept) and the device error word reads ERR_BAD_PAGE (0x700).
  * Only B, S, Hkv, D, Lmax, n_layers of dims are read. Errors: TD_ERR_INVALID_ARG (null or
  * misaligned pointers, Lmax < S, a malformed td_paging). Asynchronous on stream; no
  * workspace. */
 td_status td_kv_append(const td_dims* dims, const td_layer* layers, const td_kv* block_kv,
                        int* ctx_len, const td_paging* paging, void* stream);
+
+/* adaLN-single timestep map ([chathome] inference paragraph: the diffusion timestep modulates
+ * every layer through adaLN-single, about 1.5 M parameters in all; the map from the timestep
+ * to the shared vector is not given, and this is a reading of it): the table of shared
+ * vectors phi(t), t = 1..T, that td_denoise_step and td_decode_block take:
+ *   tau = t / T, s = 1000 tau, w_j = 10000^(-j/128), j = 0..127,
+ *   e(tau) = [cos(s w_0) .. cos(s w_127), sin(s w_0) .. sin(s w_127)]   (256 values)
+ *   phi_table[t-1, r, c] = (W_t e(tau) + b_t)[r*d + c]                   (r < 6, c < d)
+ * computed in double precision and rounded to fp32 once.
+ *   w_t fp32 [6*d, 256] device   b_t fp32 [6*d] device   phi_table fp32 [T, 6, d] device (out)
+ * Errors: TD_ERR_INVALID_ARG (null pointer, d <= 0, T outside 1..65536), TD_ERR_UNSUPPORTED
+ * (6*d > 2^30). Asynchronous on stream; no workspace. */
+td_status td_timestep_table(const float* w_t, const float* b_t, int d, int T, float* phi_table,
+                            void* stream);
 
 /* Reads and clears the device error word that bounded waits write (0 = none); the
  * current device is used. Synchronises the device. Returns TD_ERR_DEVICE_TIMEOUT (with *code
@@ -304,9 +344,12 @@ td_status td_check_bounded_wait(unsigned int limit_us, void* stream);
  * Scratch: a fixed 16 MiB array in device memory that is part of this library, so every GPU
  * that loads the library holds it until the process exits. Its device address is looked up
  * on the first call made on each device (with that device current); make that first call
- * before any stream capture. Nothing is allocated, by this call or by that set-up.
- * Limit: B*S * ceil(V / N_tile) * 12 + 256 bytes must fit in 16 MiB, with N_tile = 128 for
- * B*S <= 128 and 256 otherwise (e.g. B*S <= 2048 rows at V = 131072); larger problems return
+ * before any stream capture. The address is kept for the life of the process: after a
+ * cudaDeviceReset() of that device it is stale, and this entry point must not be called on
+ * that device again. Nothing is allocated, by this call or by that set-up.
+ * Limit: 3 * align256(B*S * ceil(V / N_tile) * 4) + 256 bytes must fit in 16 MiB
+ * (align256 rounds up to a multiple of 256; N_tile = 128 for B*S <= 128, 256 otherwise).
+ * For example 2720 rows (B = 170, S = 16) at V = 131072 fit; larger problems return
  * TD_ERR_WORKSPACE with nothing launched.
  * All calls share the one array and it keeps the last call's contents (the commit counters
  * are cleared by every call): calls that can overlap on the GPU (different streams, or

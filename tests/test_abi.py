@@ -57,7 +57,7 @@ def test_workspace_sizes_and_unsupported_shapes(lib):
 def test_null_pointers_are_rejected_before_any_launch(lib):
     dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=1)
     # every pointer null: validation must fail first
-    assert lib.td_block_attention(ctypes.byref(dm), None, None, None, None, None, None, None,
+    assert lib.td_block_attention(ctypes.byref(dm), None, None, None, None, None, None, None, 0,
                                   None, None, None, 0, None) == 1
     assert lib.td_lmhead_commit(ctypes.byref(dm), None, None, 0.8, 0, 0, None, None, None, None,
                                 None, None, None, 0, None) == 1
@@ -70,7 +70,7 @@ def test_null_pointers_are_rejected_before_any_launch(lib):
     # shapes outside the kernels' limits
     bad = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=80, V=1024, Lmax=64, n_layers=1)
     fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the shape check fails first
-    assert lib.td_block_attention(ctypes.byref(bad), fake, fake, fake, fake, fake, None, None,
+    assert lib.td_block_attention(ctypes.byref(bad), fake, fake, fake, fake, fake, None, None, 0,
                                   fake, None, fake, 1 << 20, None) == 3
 
 
@@ -78,7 +78,7 @@ def test_null_pointers_are_rejected_before_any_launch(lib):
 def test_undersized_workspace_is_rejected(lib):
     dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=1)
     fake = ctypes.c_void_p(1 << 40)
-    assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None, None,
+    assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None, None, 0,
                                   fake, None, fake, 16, None) == 2
 
 
@@ -94,7 +94,8 @@ def test_invalid_step_options_are_rejected(lib):
     fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the option check fails first
     steps = ctypes.c_int(0)
     for opts in (td.td_step_opts(5, 0.0), td.td_step_opts(0, -1.0),
-                 td.td_step_opts(0, float("nan"))):
+                 td.td_step_opts(0, float("nan")),
+                 td.td_step_opts(0, 0.0, td.td_paging(), None, 2)):   # unknown precision
         assert lib.td_denoise_step(ctypes.byref(dm), None, None, fake, fake, fake, fake, fake, 1,
                                    16, 0.8, ctypes.byref(opts), fake, fake, fake, fake, fake,
                                    fake, fake, 1 << 30, None) == 1
@@ -109,7 +110,8 @@ def test_malformed_paging_is_rejected(lib):
     for pg in (td.td_paging(fake, 2, 8),     # 2 columns cannot cover Lmax = 300 (3 tiles)
                td.td_paging(fake, 3, 0)):    # empty pool
         assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None,
-                                      ctypes.byref(pg), fake, None, fake, 1 << 30, None) == 1
+                                      ctypes.byref(pg), 0, fake, None, fake, 1 << 30,
+                                      None) == 1
         assert lib.td_kv_append(ctypes.byref(dm), None, None, fake, ctypes.byref(pg), None) == 1
 
 
@@ -169,3 +171,34 @@ def test_workspace_sizes_grow_with_the_problem():
     assert step >= ws(td.TD_FN_LMHEAD_COMMIT) and step >= ws(td.TD_FN_BLOCK_ATTENTION)
     # the loop runs the step: the same workspace
     assert ws(td.TD_FN_DECODE_BLOCK) == step
+
+
+def test_timestep_table_validates_on_the_host(lib):
+    p = ctypes.c_void_p(16)   # never dereferenced: every call below is rejected first
+    assert lib.td_timestep_table(None, p, 64, 16, p, None) == 1
+    assert lib.td_timestep_table(p, p, 0, 16, p, None) == 1
+    assert lib.td_timestep_table(p, p, 64, 0, p, None) == 1
+    assert lib.td_timestep_table(p, p, 64, 65537, p, None) == 1
+    assert lib.td_timestep_table(p, p, 1 << 28, 16, p, None) == 3
+
+
+def test_decode_block_rejects_a_final_state_output(lib):
+    dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=0)
+    p = ctypes.c_void_p(256)
+    opts = td.td_step_opts(0, 0.0, td.td_paging(), 256)
+    steps = ctypes.c_int(0)
+    assert lib.td_decode_block(ctypes.byref(dm), None, None, p, p, p, p, 1, 16, 0.8,
+                               ctypes.byref(opts), p, p, p, p, p, p, ctypes.byref(steps), p,
+                               1 << 30, None) == 1
+    # a misaligned final-state buffer is rejected by the step too
+    opts.h_out = 258
+    assert lib.td_denoise_step(ctypes.byref(dm), None, None, None, p, p, p, p, 1, 16, 0.8,
+                               ctypes.byref(opts), p, p, p, p, p, p, p, 1 << 30, None) == 1
+
+
+def test_unknown_attention_precision_is_rejected(lib):
+    dm = td.make_dims(B=1, S=16, d=256, Hq=4, Hkv=1, D=64, V=1024, Lmax=64, n_layers=1)
+    fake = ctypes.c_void_p(1 << 40)   # never dereferenced: the precision check fails first
+    for bad in (2, -1):
+        assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None, None,
+                                      bad, fake, None, fake, 1 << 30, None) == 1

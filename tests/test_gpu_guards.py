@@ -10,9 +10,8 @@ import pytest
 import torch
 
 import block_diffusion_lm_denoise_b300 as td
-import oracle
 from block_diffusion_lm_denoise_b300 import synth
-from parity_util import STACKED_CONF_BAND, compare_commit, runner_up_ties
+from parity_util import stacked_step_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -81,15 +80,10 @@ def test_step_at_odd_shapes_writes_only_its_outputs_and_matches_oracle(cuda_devi
     assert td.td_device_error() == 0
     for g in (g_tok, g_msk, g_conf, g_pred, g_ncom, g_done, g_ws):
         assert g.intact()
-    cpu_layers = [{k: v.cpu() for k, v in L.items()} for L in layers]
-    m0 = masked0.cpu().numpy().astype(bool)
-    r = oracle.denoise_step(dm.as_dict(), cpu_layers, phi[1].cpu(), w_lm.cpu(),
-                            tok0.cpu().numpy(), m0, 0.8, 2, 16, emb=emb.cpu(), pos=pos.cpu(),
-                            ctx_len=ctx)
-    ties = runner_up_ties(r["h_final"], w_lm.cpu(), g_pred.t.cpu().numpy(), r["pred"], r["gap"], m0)
-    compare_commit(r, dict(conf=g_conf.t.cpu().numpy(), pred=g_pred.t.cpu().numpy(),
-                           tokens=g_tok.t.cpu().numpy(), masked=g_msk.t.cpu().numpy()),
-                   m0, 0.8, step=True, tie_extra=ties, conf_band=STACKED_CONF_BAND)
+    stacked_step_parity(dm.as_dict(), layers, w_lm, phi[1], 2, 16, 0.8, tok0, masked0,
+                        dict(conf=g_conf.t.cpu().numpy(), pred=g_pred.t.cpu().numpy(),
+                             tokens=g_tok.t.cpu().numpy(), masked=g_msk.t.cpu().numpy()),
+                        emb=emb, pos=pos, ctx_len=ctx)
 
 
 def test_attention_lmhead_and_append_write_only_their_outputs(cuda_device):

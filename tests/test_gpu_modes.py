@@ -11,7 +11,7 @@ import torch
 import block_diffusion_lm_denoise_b300 as td
 import oracle
 from block_diffusion_lm_denoise_b300 import synth
-from parity_util import STACKED_CONF_BAND, attention_close, compare_commit, first_masked, runner_up_ties
+from parity_util import attention_close, compare_commit, first_masked, stacked_step_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -136,8 +136,9 @@ def test_kv_append_matches_oracle_and_flags_overflow(cuda_device):
 def test_three_blocks_with_the_cache_growing_between_them(cuda_device):
     # multi-block generation: decode a block, append the context tower's keys / values of the
     # committed block (a seeded per-token stand-in for that tower), decode the next block.
-    # Every step is compared with the oracle fed the GPU's state before that step, so a
-    # near-tie decision (excluded by the shared rules) cannot hide later mismatches.
+    # Every step is compared with the oracle fed the GPU's state before that step (stage by
+    # stage: layers, then LM head and commit on the GPU's final hidden state), so a near-tie
+    # decision (excluded by the shared rules) cannot hide later mismatches.
     dm = synth.Dims(B=3, S=16, d=256, Hq=8, Hkv=2, D=128, V=2048, Lmax=90 + 3 * 16,
                     n_layers=2)
     layers, w_lm, emb, pos, phi = _small_model(61, dm, cuda_device, w_scale=0.08)
@@ -156,19 +157,16 @@ def test_three_blocks_with_the_cache_growing_between_them(cuda_device):
         # step by step through td_denoise_step, each step checked against the oracle
         tk, mk = tokens.clone(), masked.clone()
         for t in range(1, dm.S + 1):
-            t_before, m_before = tk.cpu().numpy(), mk.cpu().numpy().astype(bool)
+            t_before, m_before = tk.clone(), mk.clone()
             conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[t - 1],
                                                         t, dm.S, 0.8, tk, mk, emb=emb, pos=pos,
                                                         ctx_len=ctx, ws=ws)
-            r = oracle.denoise_step(dm.as_dict(), cpu_layers, phi[t - 1].cpu(), w_lm.cpu(),
-                                    t_before, m_before, 0.8, t, dm.S, emb=emb.cpu(),
-                                    pos=pos.cpu(), ctx_len=ctx_ref)
-            ties = runner_up_ties(r["h_final"], w_lm.cpu(), pred.cpu().numpy(), r["pred"],
-                                  r["gap"], m_before)
-            compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
-                                   tokens=tk.cpu().numpy(), masked=mk.cpu().numpy()),
-                           m_before, 0.8, step=True, tie_extra=ties,
-                           conf_band=STACKED_CONF_BAND)
+            torch.cuda.synchronize()
+            stacked_step_parity(dm.as_dict(), layers, w_lm, phi[t - 1], t, dm.S, 0.8, t_before,
+                                m_before, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                                               tokens=tk.cpu().numpy(),
+                                               masked=mk.cpu().numpy()),
+                                emb=emb, pos=pos, ctx_len=ctx_ref)
             if int(done.item()):
                 break
         # the loop entry point reproduces the step-by-step run bit for bit
@@ -213,14 +211,14 @@ def test_denoise_step_rotary_variant_matches_oracle(cuda_device, Hq, D):
     assert td.td_device_error() == 0
     cpu_layers = [{k: v.cpu() for k, v in L.items()} for L in layers]
     m0n = m0.cpu().numpy().astype(bool)
+    stacked_step_parity(dm.as_dict(), layers, w_lm, phi[2], 3, 16, 0.8, t0, m0,
+                        dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                             tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
+                        emb=emb, pos=pos, ctx_len=[150, 61, 0], rope_theta=theta)
+    # the rotation changes the result: the same step without it differs
     r = oracle.denoise_step(dm.as_dict(), cpu_layers, phi[2].cpu(), w_lm.cpu(), t0.cpu().numpy(),
                             m0n, 0.8, 3, 16, emb=emb.cpu(), pos=pos.cpu(), ctx_len=[150, 61, 0],
                             rope_theta=theta)
-    ties = runner_up_ties(r["h_final"], w_lm.cpu(), pred.cpu().numpy(), r["pred"], r["gap"], m0n)
-    compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
-                           tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
-                   m0n, 0.8, step=True, tie_extra=ties, conf_band=STACKED_CONF_BAND)
-    # the rotation changes the result: the same step without it differs
     r0 = oracle.denoise_step(dm.as_dict(), cpu_layers, phi[2].cpu(), w_lm.cpu(), t0.cpu().numpy(),
                              m0n, 0.8, 3, 16, emb=emb.cpu(), pos=pos.cpu(), ctx_len=[150, 61, 0])
     assert np.abs(r0["conf"] - r["conf"]).max() > 1e-4

@@ -14,7 +14,7 @@ import torch
 import block_diffusion_lm_denoise_b300 as td
 import oracle
 from block_diffusion_lm_denoise_b300 import synth
-from parity_util import attention_close, compare_commit
+from parity_util import attention_close, compare_commit, oracle_layers, stacked_step_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -102,6 +102,41 @@ def test_block_attention_matches_oracle(cuda_device, B, S, Hq, Hkv, D, Lmax, ctx
         assert torch.equal(o[0, 0, 0], vb[0, 0, 0]) and torch.equal(o[0, 0, 3], vb[0, 0, 0])
 
 
+# the probabilities carried as hi + lo bf16 pairs: the output is the oracle's, rounded to bf16,
+# except where the fp32 sums land within about 1e-6 of a bf16 rounding boundary (one step)
+SPLIT_CASES = [(2, 16, 32, 2, 128, 300, None), (3, 16, 32, 2, 128, 4000, [4000, 1234, 0]),
+               (3, 16, 8, 2, 128, 200, [200, 0, 77]), (4, 16, 16, 4, 64, 2000, None),
+               (2, 48, 32, 2, 128, 260, None)]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,D,Lmax,ctx", SPLIT_CASES)
+def test_block_attention_split_probabilities_round_like_the_oracle(cuda_device, B, S, Hq, Hkv,
+                                                                  D, Lmax, ctx):
+    seed = 13
+    q = synth.normal((B, S, Hq, D), 1.0, seed, "q", cuda_device)
+    kb = synth.normal((B, S, Hkv, D), 1.0, seed, "kb", cuda_device)
+    vb = synth.normal((B, S, Hkv, D), 1.0, seed, "vb", cuda_device)
+    kc = synth.normal((B, Hkv, Lmax, D), 1.0, seed, "kc", cuda_device)
+    vc = synth.normal((B, Hkv, Lmax, D), 1.0, seed, "vc", cuda_device)
+    ctx_t = None if ctx is None else torch.tensor(ctx, dtype=torch.int32, device=cuda_device)
+    dims = td.make_dims(B=B, S=S, d=64, Hq=Hq, Hkv=Hkv, D=D, V=8, Lmax=Lmax, n_layers=1)
+    o16 = td.td_block_attention(dims, q, kb, vb, kc, vc, ctx_t)
+    o = td.td_block_attention(dims, q, kb, vb, kc, vc, ctx_t, precision=td.TD_ATTN_P_SPLIT)
+    torch.cuda.synchronize()
+    _no_device_error()
+    o_ref, _ = oracle.block_attention(q, kb, vb, kc, vc, ctx)
+    ref = oracle.bf16_round(o_ref)
+    got = _np(o)
+    # one bf16 step of the value, plus the fp32 accumulation error of a sum whose terms are of
+    # the row's size (it dominates where the terms cancel to a value near zero)
+    step = np.abs(ref) * 2.0**-7 + 1e-5 * np.abs(ref).max(axis=-1, keepdims=True)
+    assert (np.abs(got - ref) <= step).all(), float((np.abs(got - ref) - step).max())
+    exact = float((got == ref).mean())
+    exact16 = float((_np(o16) == ref).mean())
+    print("exact bf16 outputs: split", exact, "bf16 P", exact16)
+    assert exact >= 0.99 and exact > exact16
+
+
 @pytest.mark.parametrize("L", [512, 2048, 8192, 32768])
 def test_attention_sweep_full_size_sampled(cuda_device, L):
     wl = synth.attention_sweep(L, cuda_device)
@@ -184,9 +219,30 @@ def test_lmhead_gamma_above_one_commits_lowest_index_of_identical_rows(cuda_devi
     assert int(done.item()) == 0
 
 
-@pytest.mark.parametrize("M,S,gamma", [(16, 16, 0.8), (256, 4, 0.5), (1024, 16, 0.8),
-                                       (4096, 32, 0.95)])
+# Row r of the LM-head sweep's hidden states and weights does not depend on M or S (the
+# generator is per element), so the oracle's per-row results are computed once and shared by
+# the whole grid.
+_LM_ROWS = {}
+
+
+def _lm_oracle_rows(wl, rows):
+    need = [r for r in rows if r not in _LM_ROWS]
+    if need:
+        c, p, g, _ = oracle.lmhead_confidence(wl.h, wl.w_lm, rows=need)
+        for r, ci, pi, gi in zip(need, c, p, g):
+            _LM_ROWS[r] = (ci, pi, gi)
+    got = [_LM_ROWS[r] for r in rows]
+    return (np.array([x[0] for x in got]), np.array([x[1] for x in got]),
+            np.array([x[2] for x in got]))
+
+
+LM_GRID = [(M, S, g) for M in (16, 256, 1024, 4096) for S in (4, 16, 32) if S <= M
+           for g in (0.5, 0.8, 0.95)]
+
+
+@pytest.mark.parametrize("M,S,gamma", LM_GRID)
 def test_lmhead_sweep_full_size_sampled(cuda_device, M, S, gamma):
+    # the LM-head sweep's whole grid: rows M x block size S x threshold gamma
     wl = synth.lmhead_sweep(M, S, gamma, cuda_device)
     dm = wl.dims
     t0 = wl.tokens.clone()
@@ -197,7 +253,7 @@ def test_lmhead_sweep_full_size_sampled(cuda_device, M, S, gamma):
     _no_device_error()
     seqs = sorted({0, dm.B // 2, dm.B - 1})
     rows = [b * S + i for b in seqs for i in range(S)]
-    c_ref, p_ref, gap, _ = oracle.lmhead_confidence(wl.h, wl.w_lm, rows=rows)
+    c_ref, p_ref, gap = _lm_oracle_rows(wl, rows)
     nb = len(seqs)
     tok_ref, msk_ref, _, _ = oracle.commit(c_ref.reshape(nb, S), p_ref.reshape(nb, S),
                                            t0[seqs].cpu().numpy(),
@@ -266,12 +322,11 @@ def test_denoise_step_embed_path_and_stacked_layers(cuda_device):
                                                 tokens, masked, emb=emb, pos=pos, ctx_len=ctx)
     torch.cuda.synchronize()
     _no_device_error()
-    r = oracle.denoise_step(dm.as_dict(), layers, phi[4], w_lm, t0.cpu().numpy(),
-                            m0.cpu().numpy().astype(bool), 0.8, 5, 16, emb=emb, pos=pos,
-                            ctx_len=[200, 64, 13])
-    compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
-                           tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
-                   m0.cpu().numpy(), 0.8, step=True)
+    rep = stacked_step_parity(dm.as_dict(), layers, w_lm, phi[4], 5, 16, 0.8, t0, m0,
+                              dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                                   tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
+                              emb=emb, pos=pos, ctx_len=[200, 64, 13])
+    print(rep)
 
 
 @pytest.mark.parametrize("n_layers", [0, 2])
@@ -296,11 +351,9 @@ def test_denoise_step_evaluates_only_rows_masked_at_step_start(cuda_device, n_la
                                                 tokens, masked, h=h)
     torch.cuda.synchronize()
     _no_device_error()
-    r = oracle.denoise_step(dm.as_dict(), layers, phi[2], w_lm, t0.cpu().numpy(),
-                            m0.cpu().numpy().astype(bool), 0.8, 3, 16, h=h)
-    compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
-                           tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()),
-                   m0.cpu().numpy(), 0.8, step=True)
+    stacked_step_parity(dm.as_dict(), layers, w_lm, phi[2], 3, 16, 0.8, t0, m0,
+                        dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                             tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy()), h=h)
     assert ncom[1].item() == 0 and ncom[2].item() == 1 and ncom[0].item() >= 1
     assert torch.equal(tokens[1], t0[1])
     # nothing masked at all: no row is evaluated, nothing commits, the block is done
@@ -326,24 +379,32 @@ def test_denoise_step_mid_size(cuda_device):
     rep = compare_commit(r, dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
                                  tokens=wl.tokens.cpu().numpy(), masked=wl.masked.cpu().numpy()),
                          m0.cpu().numpy(), wl.gamma, step=True)
-    frac = float((r["conf"][m0.cpu().numpy().astype(bool)] >= 0.8).mean())
-    print("mid step:", rep, "fraction of masked rows with conf >= 0.8:", frac)
+    # the workload's defining property: about 30 % of the masked rows clear gamma = 0.8
+    # (tests/golden/calibrate_mid_scale.py: 0.302 in the oracle), in the oracle and on the GPU
+    m0n = m0.cpu().numpy().astype(bool)
+    frac = float((r["conf"][m0n] >= 0.8).mean())
+    frac_gpu = float((conf.cpu().numpy()[m0n] >= 0.8).mean())
+    print("mid step:", rep, "fraction of masked rows with conf >= 0.8:", frac, frac_gpu)
+    assert 0.25 <= frac <= 0.35 and abs(frac_gpu - frac) <= 2.0 / m0n.sum()
 
 
 # ------------------------------------------------------------------------------ decode loop
 
-def _step_trace_gpu(wl, n_steps):
+def _step_trace_gpu(wl):
+    """The block decode run step by step through td_denoise_step; per step the state before
+    it and its outputs."""
     dm = wl.dims
     tokens = wl.tokens.clone()
     masked = wl.masked.clone()
     ws = td.workspace(dm.as_dict(), td.TD_FN_DENOISE_STEP)
     trace = []
     for t in range(1, wl.T + 1):
+        before = (tokens.clone(), masked.clone())
         conf, pred, ncom, done = td.td_denoise_step(dm.as_dict(), wl.layers, wl.w_lm,
                                                     wl.phi_table[t - 1], t, wl.T, wl.gamma,
                                                     tokens, masked, emb=wl.emb, pos=wl.pos,
                                                     ws=ws)
-        trace.append(dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+        trace.append(dict(before=before, conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
                           tokens=tokens.cpu().numpy(), masked=masked.cpu().numpy(),
                           n=ncom.cpu().numpy()))
         if int(done.item()):
@@ -351,10 +412,14 @@ def _step_trace_gpu(wl, n_steps):
     return trace
 
 
-def test_decode_loop_full_size_sampled(cuda_device):
-    wl = synth.decode_loop(cuda_device)
+# the decode workload at its two logit scales: W_lm sigma 0.02 (confidences stay below every
+# threshold: one commit per sequence and step) and the calibrated scale of the bench line
+# (several commits per step early in the block)
+@pytest.mark.parametrize("w_lm_sigma", [0.02, synth.DECODE_W_LM_SIGMA])
+def test_decode_loop_full_size_sampled(cuda_device, w_lm_sigma):
+    wl = synth.decode_loop(cuda_device, w_lm_sigma=w_lm_sigma)
     dm = wl.dims
-    trace = _step_trace_gpu(wl, wl.T)
+    trace = _step_trace_gpu(wl)
     _no_device_error()
     # the loop entry point reproduces the step-by-step run bit for bit
     tokens, masked = wl.tokens.clone(), wl.masked.clone()
@@ -364,29 +429,52 @@ def test_decode_loop_full_size_sampled(cuda_device):
     assert steps == len(trace)
     assert np.array_equal(tokens.cpu().numpy(), trace[-1]["tokens"])
     assert not masked.any()
-    # invariants over the whole batch
+    # invariants over the whole batch: at least one commit per live sequence and step, no
+    # committed position reverts
     prev = np.ones((dm.B, dm.S), bool)
     for rec in trace:
         live = prev.any(axis=1)
         assert (rec["n"][live] >= 1).all()
         assert not (rec["masked"].astype(bool) & ~prev).any()
         prev = rec["masked"].astype(bool)
-    # oracle on two sampled sequences, step by step, until an excluded decision
-    seqs = [0, dm.B - 1]
-    sub = [{k: v.cpu() for k, v in L.items()} for L in _oracle_layers(wl, seqs)]
-    w_cpu, emb_cpu, pos_cpu, phi_cpu = wl.w_lm.cpu(), wl.emb.cpu(), wl.pos.cpu(), wl.phi_table.cpu()
-    dsub = dict(dm.as_dict(), B=len(seqs))
-    tok = np.full((len(seqs), dm.S), dm.V)
-    msk = np.ones((len(seqs), dm.S), bool)
+    if w_lm_sigma == 0.02:
+        assert len(trace) == dm.S and all((rec["n"] == 1).all() for rec in trace)
+    else:
+        # confidence masking commits several positions per sequence in the first step
+        assert trace[0]["n"].sum() > 2 * dm.B and len(trace) < dm.S
+    # every step against the oracle on four sampled sequences, stage by stage; in the first
+    # step also against the oracle's own step from the same inputs (conf within 2e-3). With
+    # the calibrated (sharper) logits, six stacked layers of bf16 probabilities in P V move the
+    # conf of the oracle's own step by about the bar: there the end-to-end figure is reported
+    # for the default arithmetic and asserted with the probabilities carried as hi + lo.
+    seqs = [0, 21, 42, dm.B - 1]
+    cpu_layers = oracle_layers(wl.layers, seqs)
+    compared = 0
+    sharp = w_lm_sigma != 0.02
     for t, rec in enumerate(trace, start=1):
-        r = oracle.denoise_step(dsub, sub, phi_cpu[t - 1], w_cpu, tok, msk, wl.gamma,
-                                t, wl.T, emb=emb_cpu, pos=pos_cpu)
-        rep = compare_commit(r, dict(conf=rec["conf"][seqs], pred=rec["pred"][seqs],
-                                     tokens=rec["tokens"][seqs], masked=rec["masked"][seqs]),
-                             msk, wl.gamma, step=True)
-        if rep["excluded_sequences"]:
-            print("decode loop: stopped comparing at step", t, rep)
-            break
-        tok, msk = r["tokens"], r["masked"]
-        if not msk.any():
-            break
+        tb, mb = rec["before"]
+        rep = stacked_step_parity(dm.as_dict(), wl.layers, wl.w_lm, wl.phi_table[t - 1], t,
+                                  wl.T, wl.gamma, tb, mb,
+                                  dict(conf=rec["conf"], pred=rec["pred"], tokens=rec["tokens"],
+                                       masked=rec["masked"]),
+                                  emb=wl.emb, pos=wl.pos, seqs=seqs,
+                                  end_to_end=(("report" if sharp else True) if t == 1 else False),
+                                  cpu_layers=cpu_layers)
+        if t == 1:
+            print("decode loop, step 1, P in bf16:", rep)
+        compared += 1
+    assert compared == len(trace) == steps
+    if sharp:
+        tb, mb = trace[0]["before"]
+        tk, mk = tb.clone(), mb.clone()
+        conf, pred, _, _ = td.td_denoise_step(dm.as_dict(), wl.layers, wl.w_lm, wl.phi_table[0],
+                                              1, wl.T, wl.gamma, tk, mk, emb=wl.emb, pos=wl.pos,
+                                              attn_precision=td.TD_ATTN_P_SPLIT)
+        torch.cuda.synchronize()
+        rep = stacked_step_parity(dm.as_dict(), wl.layers, wl.w_lm, wl.phi_table[0], 1, wl.T,
+                                  wl.gamma, tb, mb,
+                                  dict(conf=conf.cpu().numpy(), pred=pred.cpu().numpy(),
+                                       tokens=tk.cpu().numpy(), masked=mk.cpu().numpy()),
+                                  emb=wl.emb, pos=wl.pos, seqs=seqs, end_to_end=True,
+                                  cpu_layers=cpu_layers, attn_precision=td.TD_ATTN_P_SPLIT)
+        print("decode loop, step 1, P as hi + lo:", rep)

@@ -13,8 +13,9 @@ import pytest
 import torch
 
 import block_diffusion_lm_denoise_b300 as td
+import oracle
 from block_diffusion_lm_denoise_b300 import synth
-from parity_util import CONF_TOL
+from parity_util import CONF_TOL, compare_commit
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +40,10 @@ def _call_static(dims, h, w, gamma, tokens, masked, conf, pred, ncom, done):
     assert st == 0, lib.td_status_string(st).decode()
 
 
-@pytest.mark.parametrize("M,S,V,d", [(256, 16, 4096, 512), (1024, 16, 131072, 4096)])
+# the last case is the largest row count whose partials fit the 16 MiB scratch at this
+# vocabulary: 3 * 2720 * 512 * 4 + 256 bytes
+@pytest.mark.parametrize("M,S,V,d", [(256, 16, 4096, 512), (1024, 16, 131072, 4096),
+                                     (2720, 16, 131072, 4096)])
 def test_static_scratch_matches_workspace_entry_twice(cuda_device, M, S, V, d):
     gamma = 0.8
     h, w, tokens0, masked0 = _case(cuda_device, M, S, V, d, seed=31)
@@ -62,6 +66,20 @@ def test_static_scratch_matches_workspace_entry_twice(cuda_device, M, S, V, d):
         assert torch.equal(pred, p_ref)
         assert torch.equal(tok, t_ref) and torch.equal(msk, m_ref)
         assert torch.equal(ncom, n_ref) and torch.equal(done, d_ref)
+    # and against the fp64 oracle on three sampled sequences
+    B = M // S
+    seqs = sorted({0, B // 2, B - 1})
+    rows = [b * S + i for b in seqs for i in range(S)]
+    c, p, gap, _ = oracle.lmhead_confidence(h, w, rows=rows)
+    nb = len(seqs)
+    m0 = masked0[seqs].cpu().numpy().astype(bool)
+    tok_o, msk_o, _, _ = oracle.commit(c.reshape(nb, S), p.reshape(nb, S),
+                                       tokens0[seqs].cpu().numpy(), m0, gamma, False)
+    compare_commit(dict(conf=c.reshape(nb, S), pred=p.reshape(nb, S), gap=gap.reshape(nb, S),
+                        tokens=tok_o, masked=msk_o),
+                   dict(conf=conf[seqs].cpu().numpy(), pred=pred[seqs].cpu().numpy(),
+                        tokens=tok[seqs].cpu().numpy(), masked=msk[seqs].cpu().numpy()),
+                   m0, gamma)
 
 
 def test_static_scratch_rejects_problems_beyond_its_size(cuda_device):
