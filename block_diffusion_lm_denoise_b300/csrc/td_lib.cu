@@ -238,11 +238,36 @@ td_status launch_gemm(const void* A, const void* Bm, int M, int N, int K, GemmPa
   return TD_OK;
 }
 
+// 256 x 256 tiles on SM pairs: grid = two CTAs per pair tile, at most one pair per TPC.
+template <int STAGES, int EPI>
+td_status launch_gemm_pair(const void* A, const void* Bm, int M, int N, int K, GemmParams gp,
+                           cudaStream_t st, int nsm) {
+  using L = GemmPairSmem<STAGES>;
+  CUtensorMap ma, mb;
+  const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)K * 2};
+  const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)K * 2};
+  const uint32_t box[2] = {64, 128};
+  if (!make_map(&ma, A, 2, da, sa, box) || !make_map(&mb, Bm, 2, db, sb, box)) return TD_ERR_CUDA;
+  gp.M = M;
+  gp.N = N;
+  gp.K = K;
+  gp.m_tiles = (M + 255) / 256;
+  gp.n_tiles = (N + 255) / 256;
+  gp.items = gp.m_tiles * gp.n_tiles;
+  auto kern = gemm_pair_kernel<STAGES, EPI>;
+  TD_CUDA(set_smem(kern, L::kBytes));
+  const int grid = 2 * std::min(gp.items, std::max(1, nsm / 2));
+  kern<<<grid, 256, L::kBytes, st>>>(ma, mb, gp);
+  TD_CUDA(cudaGetLastError());
+  return TD_OK;
+}
+
+// bn = 128: single-CTA 128 x 128 tiles (few rows); bn = 256: 256 x 256 tiles on SM pairs.
 template <int EPI>
 td_status gemm_dispatch(const void* A, const void* Bm, int M, int N, int K, GemmParams gp,
                         cudaStream_t st, int nsm, int bn) {
   if (bn == 128) return launch_gemm<128, 6, EPI>(A, Bm, M, N, K, gp, st, nsm);
-  return launch_gemm<256, 4, EPI>(A, Bm, M, N, K, gp, st, nsm);
+  return launch_gemm_pair<kPairGemmStages, EPI>(A, Bm, M, N, K, gp, st, nsm);
 }
 
 // adaLN-single modulation: the column-slab path for d = 256 * k (d <= 8192) with 16-byte
@@ -555,11 +580,12 @@ void set_all_smem() {
   set_smem(gemm_tn_kernel<128, 6, EPI_QKV>, GemmSmem<128, 6>::kBytes);
   set_smem(gemm_tn_kernel<128, 6, EPI_RESID>, GemmSmem<128, 6>::kBytes);
   set_smem(gemm_tn_kernel<128, 6, EPI_LMHEAD>, GemmSmem<128, 6>::kBytes);
-  set_smem(gemm_tn_kernel<256, 4, EPI_QKV>, GemmSmem<256, 4>::kBytes);
-  set_smem(gemm_tn_kernel<256, 4, EPI_RESID>, GemmSmem<256, 4>::kBytes);
-  set_smem(gemm_tn_kernel<256, 4, EPI_LMHEAD>, GemmSmem<256, 4>::kBytes);
   set_smem(gemm_tn_kernel<128, 6, EPI_QKV_ROPE>, GemmSmem<128, 6>::kBytes);
-  set_smem(gemm_tn_kernel<256, 4, EPI_QKV_ROPE>, GemmSmem<256, 4>::kBytes);
+  using GP = GemmPairSmem<kPairGemmStages>;
+  set_smem(gemm_pair_kernel<kPairGemmStages, EPI_QKV>, GP::kBytes);
+  set_smem(gemm_pair_kernel<kPairGemmStages, EPI_RESID>, GP::kBytes);
+  set_smem(gemm_pair_kernel<kPairGemmStages, EPI_LMHEAD>, GP::kBytes);
+  set_smem(gemm_pair_kernel<kPairGemmStages, EPI_QKV_ROPE>, GP::kBytes);
   set_smem(attn_fused_kernel<128, false, false>, AttnSmem<128>::kBytes);
   set_smem(attn_fused_kernel<64, false, false>, AttnSmem<64>::kBytes);
   set_smem(attn_pair_kernel<false, false>, PairSmem::kBytes);

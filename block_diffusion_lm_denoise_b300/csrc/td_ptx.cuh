@@ -401,6 +401,15 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
 
 // TMA load into this CTA's shared memory whose byte count completes on an mbarrier given by
 // its shared::cluster address (the even CTA's barrier of the pair).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster_addr, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster_addr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map,
                                                  uint32_t bar_cluster_addr, int c0, int c1,
                                                  int c2) {
