@@ -247,6 +247,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--loop-graph", default="conditional", choices=["conditional", "flat"],
+                    help="form of the decode-loop graph (ncu's launch list sees the kernels "
+                         "of the flat form only)")
     ap.add_argument("--only", choices=["attention", "lmhead", "step"],
                     help="launch one kernel family alone, or one denoise step of one layer "
                          "(for profiler captures)")
@@ -274,6 +277,8 @@ def main():
 
     import block_diffusion_lm_denoise_b300 as td
     td.lib()   # fails loudly if the CUDA library is missing
+    if args.loop_graph == "flat":
+        td.td_decode_graph_form(td.TD_GRAPH_FLAT)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = synth.decode_loop(dev, seed=4 + rank, w_lm_sigma=synth.DECODE_W_LM_SIGMA)
@@ -506,10 +511,12 @@ def main():
                "clocks": lclocks.summary(lm_ms * l_reps)}
     dominant, other = (roof_attn, roof_lm) if attn_share >= lm_share else (roof_lm, roof_attn)
 
-    # embed, LM row map, 6 x (adaLN, QKV, attention, O-proj), LM head, commit; the block's
-    # graph holds the kernels of all T steps and launches every one of them (those after the
-    # step that finished the block return at once)
+    # embed, LM row map, 6 x (adaLN, QKV, attention, O-proj), LM head, commit per step; with
+    # the loop graph's conditional nodes only the steps that ran launch anything, with the
+    # flat graph every step of T launches (those after the block finished return at once)
     launches_per_step = 2 + dm.n_layers * 4 + 2
+    graph_form = td.td_decode_graph_form()
+    steps_launched = total_steps if graph_form == td.TD_GRAPH_CONDITIONAL else wl.T * args.steps
     result = {
         "metric": "committed tokens/sec (block decode, S=16, gamma=0.8)",
         "value": round(value, 1),
@@ -539,7 +546,8 @@ def main():
                               "frac": round(attn_bytes / (split_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
                               "clocks": sclocks.summary(split_ms * s_reps)},
         "commit_sweep": sweep,
-        "gpu_launches": launches_per_step * wl.T * args.steps,
+        "gpu_launches": launches_per_step * steps_launched,
+        "loop_graph": "conditional" if graph_form == td.TD_GRAPH_CONDITIONAL else "flat",
         "clocks": clocks.summary(ms),
         "roofline": dominant,
         "roofline_other": other,

@@ -32,7 +32,7 @@ TD_ATTN_P_SPLIT = 1   # carried as a hi + lo pair of bf16 values (a second P V p
 EXPORTED = ("td_workspace_size", "td_status_string", "td_adaln_modulate", "td_block_attention",
             "td_lmhead_commit", "td_denoise_step", "td_decode_block", "td_device_error",
             "td_lmhead_commit_static", "td_kv_append", "td_check_bounded_wait",
-            "td_timestep_table")
+            "td_timestep_table", "td_decode_graph_form")
 
 
 class TdError(RuntimeError):
@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
         L.td_device_error.argtypes = [ctypes.POINTER(i)]
         L.td_check_bounded_wait.argtypes = [ctypes.c_uint, vp]
         L.td_timestep_table.argtypes = [vp, vp, i, i, vp, vp]
+        L.td_decode_graph_form.argtypes = [i]
         L.td_lmhead_commit_static.argtypes = [ctypes.POINTER(td_dims), vp, vp, f, i, vp, vp, vp,
                                                vp, vp, vp, vp]
         for name in EXPORTED:
@@ -343,6 +344,16 @@ def td_check_bounded_wait(limit_us: int, stream=None) -> None:
     """Launches the bounded-wait diagnostic (see include/td.h); read the result with
     td_device_error()."""
     _check("td_check_bounded_wait", lib().td_check_bounded_wait(int(limit_us), _stream(stream)))
+
+
+TD_GRAPH_CONDITIONAL = 1   # decode-loop graph: one conditional node per step
+TD_GRAPH_FLAT = 2          # decode-loop graph: one flat capture, finished steps return at once
+
+
+def td_decode_graph_form(form: int = 0) -> int:
+    """Diagnostic (see include/td.h): form 1 or 2 selects the form of decode-loop graphs built
+    from now on; returns the form of the last graph built (0 before the first)."""
+    return int(lib().td_decode_graph_form(int(form)))
 
 
 def td_timestep_table(w_t, b_t, T: int, phi_table=None, stream=None) -> torch.Tensor:

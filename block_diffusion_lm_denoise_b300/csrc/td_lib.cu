@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -289,6 +290,13 @@ td_status launch_adaln(const void* h, const float* E, const float* phi, int rows
   return TD_OK;
 }
 
+// Inside a decode-loop graph built from conditional nodes: the handle of the next step's node,
+// which the commit kernel sets to "positions left".
+struct NextStep {
+  cudaGraphConditionalHandle handle = 0;
+  int set = 0;
+};
+
 // With row_pos / m_count set, h holds only the rows masked at the step start (compacted,
 // *m_count of them on the device) and the other rows are reported as not evaluated.
 td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, float gamma,
@@ -297,7 +305,8 @@ td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, 
                             int* pred, int* n_committed, int* all_done, void* ws,
                             cudaStream_t st, int nsm, const int* skip = nullptr,
                             int* steps = nullptr, const int* row_pos = nullptr,
-                            const int* m_count = nullptr) {
+                            const int* m_count = nullptr,
+                            const NextStep& next = NextStep{}) {
   const int M = dm->B * dm->S;
   const int V = dm->V;
   const int bn = lm_bn(M);
@@ -321,7 +330,8 @@ td_status run_lmhead_commit(const td_dims* dm, const void* h, const void* w_lm, 
                                                          force_all, rule, tokens, masked, conf,
                                                          pred,
                                                          n_committed, all_done, counters,
-                                                         skip, steps, row_pos);
+                                                         skip, steps, row_pos, next.handle,
+                                                         next.set);
   TD_CUDA(cudaGetLastError());
   return TD_OK;
 }
@@ -491,7 +501,7 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
                    const td_paging* paging, int precision, int* tokens, unsigned char* masked,
                    float* conf, int* pred, int* n_committed, int* all_done, void* ws,
                    cudaStream_t st, int nsm, const int* skip = nullptr, int* steps = nullptr,
-                   void* h_out = nullptr) {
+                   void* h_out = nullptr, const NextStep& next = NextStep{}) {
   const StepWs w = carve_step(dm, ws, nsm);
   const int M = dm->B * dm->S;
   const int d = dm->d;
@@ -554,7 +564,7 @@ td_status run_step(const td_dims* dm, const td_layer* layers, const int* ctx_len
   return run_lmhead_commit(dm, w.h_lm, w_lm, gamma, rule, t == T ? 1 : 0, tokens, masked, conf,
                            pred,
                            n_committed, all_done, w.lm, st, nsm, skip, steps, w.row_pos,
-                           w.m_count);
+                           w.m_count, next);
 }
 
 td_status check_layers(const td_dims* dm, const td_layer* layers) {
@@ -573,8 +583,11 @@ td_status check_layers(const td_dims* dm, const td_layer* layers) {
 // ------------------------------------------------------------------------------------------
 // Decode loop as one CUDA graph: the T steps are captured once per distinct argument set (on
 // a private stream, since the legacy default stream cannot be captured) and replayed on the
-// caller's stream. Every kernel of step t+1 reads the all-done word that step t's commit
-// wrote and returns at once when it is set; merge_commit counts the steps that ran.
+// caller's stream. Each step sits in a conditional node that runs only while positions are
+// left (see build_loop_conditional); every kernel also reads the all-done word that the
+// previous step's commit wrote and returns at once when it is set, which is what ends the
+// loop in the flat graph used where conditional nodes are unavailable. merge_commit counts
+// the steps that ran.
 // ------------------------------------------------------------------------------------------
 void set_all_smem() {
   set_smem(gemm_tn_kernel<128, 6, EPI_QKV>, GemmSmem<128, 6>::kBytes);
@@ -606,6 +619,8 @@ struct LoopKey {
 };
 
 std::mutex g_loop_mu;
+std::atomic<int> g_loop_form_wanted{1};   // 1 conditional nodes, 2 flat
+std::atomic<int> g_loop_form_built{0};
 std::map<LoopKey, cudaGraphExec_t> g_loop_graphs;
 std::vector<LoopKey> g_loop_order;
 constexpr size_t kMaxLoopGraphs = 16;
@@ -622,6 +637,113 @@ cudaStream_t capture_stream() {
   if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
   streams[dev] = s;
   return s;
+}
+
+// The loop as a chain of conditional (if) nodes, one per step: the first step's condition
+// defaults to 1 at every launch, the others to 0, and the commit kernel of step t sets the
+// condition of step t+1 to "positions left", so the steps after the one that committed the
+// block's last position launch nothing. Each step's kernels are captured into its node's body.
+// TD_ERR_UNSUPPORTED: conditional nodes are not available (the caller builds the flat graph).
+td_status build_loop_conditional(const td_dims* dm, const td_layer* layers, const int* ctx_len,
+                                 const void* emb, const void* pos, const void* w_lm,
+                                 const float* phi_table, int t_start, int T, float gamma,
+                                 int rule, float rope_theta, const td_paging* paging,
+                                 int precision, int* tokens, unsigned char* masked, float* conf,
+                                 int* pred, int* n_committed, int* all_done, void* ws,
+                                 const StepWs& w, cudaStream_t cs, int nsm, cudaGraph_t* out) {
+  cudaGraph_t g = nullptr;
+  if (cudaGraphCreate(&g, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return TD_ERR_UNSUPPORTED;
+  }
+  std::vector<cudaGraphConditionalHandle> cond(T - t_start + 1);
+  for (int t = t_start; t <= T; ++t) {
+    if (cudaGraphConditionalHandleCreate(&cond[t - t_start], g, t == t_start ? 1u : 0u,
+                                         cudaGraphCondAssignDefault) != cudaSuccess) {
+      cudaGraphDestroy(g);
+      cudaGetLastError();
+      return TD_ERR_UNSUPPORTED;
+    }
+  }
+  cudaGraphNode_t prev = nullptr;
+  for (int t = t_start; t <= T; ++t) {
+    cudaGraphNodeParams np{};
+    np.type = cudaGraphNodeTypeConditional;
+    np.conditional.handle = cond[t - t_start];
+    np.conditional.type = cudaGraphCondTypeIf;
+    np.conditional.size = 1;
+    cudaGraphNode_t node = nullptr;
+    if (cudaGraphAddNode(&node, g, prev ? &prev : nullptr, nullptr, prev ? 1 : 0, &np) !=
+        cudaSuccess) {
+      cudaGraphDestroy(g);
+      cudaGetLastError();
+      return TD_ERR_UNSUPPORTED;
+    }
+    prev = node;
+    cudaGraph_t body = np.conditional.phGraph_out[0];
+    if (cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0,
+                                      cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      cudaGraphDestroy(g);
+      cudaGetLastError();
+      return TD_ERR_UNSUPPORTED;
+    }
+    td_status s = TD_OK;
+    if (t == t_start && (cudaMemsetAsync(all_done, 0, sizeof(int), cs) != cudaSuccess ||
+                         cudaMemsetAsync(w.loop, 0, sizeof(int), cs) != cudaSuccess))
+      s = TD_ERR_CUDA;
+    NextStep next;
+    if (t < T) {
+      next.handle = cond[t + 1 - t_start];
+      next.set = 1;
+    }
+    if (s == TD_OK)
+      s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
+                   phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, rope_theta,
+                   paging, precision, tokens, masked, conf, pred, n_committed, all_done, ws, cs,
+                   nsm, all_done, w.loop, nullptr, next);
+    cudaGraph_t captured = nullptr;
+    const cudaError_t ee = cudaStreamEndCapture(cs, &captured);
+    if (s != TD_OK || ee != cudaSuccess) {
+      cudaGraphDestroy(g);
+      cudaGetLastError();
+      return s != TD_OK ? s : TD_ERR_UNSUPPORTED;
+    }
+  }
+  *out = g;
+  return TD_OK;
+}
+
+// The loop as one flat capture of all T steps; every kernel of step t+1 reads the all-done
+// word that step t's commit wrote and returns at once when it is set.
+td_status build_loop_flat(const td_dims* dm, const td_layer* layers, const int* ctx_len,
+                          const void* emb, const void* pos, const void* w_lm,
+                          const float* phi_table, int t_start, int T, float gamma, int rule,
+                          float rope_theta, const td_paging* paging, int precision, int* tokens,
+                          unsigned char* masked, float* conf, int* pred, int* n_committed,
+                          int* all_done, void* ws, const StepWs& w, cudaStream_t cs, int nsm,
+                          cudaGraph_t* out) {
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return TD_ERR_UNSUPPORTED;
+  }
+  td_status s = TD_OK;
+  if (cudaMemsetAsync(all_done, 0, sizeof(int), cs) != cudaSuccess ||
+      cudaMemsetAsync(w.loop, 0, sizeof(int), cs) != cudaSuccess)
+    s = TD_ERR_CUDA;
+  for (int t = t_start; t <= T && s == TD_OK; ++t)
+    s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
+                 phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, rope_theta, paging,
+                 precision, tokens, masked, conf, pred, n_committed, all_done, ws, cs, nsm,
+                 all_done, w.loop);
+  cudaGraph_t g = nullptr;
+  const cudaError_t ee = cudaStreamEndCapture(cs, &g);
+  if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return s != TD_OK ? s : TD_ERR_UNSUPPORTED;
+  }
+  *out = g;
+  return TD_OK;
 }
 
 // Runs the loop through a cached graph. TD_ERR_UNSUPPORTED means "capture not possible here":
@@ -657,6 +779,8 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
   }
   u(ctx_len); u(emb); u(pos); u(w_lm); u(phi_table); u(tokens); u(masked); u(conf); u(pred);
   u(n_committed); u(all_done); u(ws);
+  const int form_wanted = g_loop_form_wanted.load();
+  key.v.push_back((uint64_t)form_wanted);
   {
     // One lock over lookup, capture, insertion and launch: no two threads capture on the
     // shared capture stream at once, a key is captured once, and no graph is destroyed
@@ -670,32 +794,30 @@ td_status decode_graph(const td_dims* dm, const td_layer* layers, const int* ctx
       set_all_smem();
       cudaStream_t cs = capture_stream();
       if (cs == nullptr) return TD_ERR_UNSUPPORTED;
-      if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
-        cudaGetLastError();
-        return TD_ERR_UNSUPPORTED;
+      // the chain of conditional nodes first; the flat capture where that cannot be built
+      // or instantiated
+      for (int flat = form_wanted == 2 ? 1 : 0; flat < 2 && exec == nullptr; ++flat) {
+        cudaGraph_t g = nullptr;
+        const td_status s =
+            flat == 0
+                ? build_loop_conditional(dm, layers, ctx_len, emb, pos, w_lm, phi_table,
+                                         t_start, T, gamma, rule, rope_theta, paging, precision,
+                                         tokens, masked, conf, pred, n_committed, all_done, ws,
+                                         w, cs, nsm, &g)
+                : build_loop_flat(dm, layers, ctx_len, emb, pos, w_lm, phi_table, t_start, T,
+                                  gamma, rule, rope_theta, paging, precision, tokens, masked,
+                                  conf, pred, n_committed, all_done, ws, w, cs, nsm, &g);
+        if (s == TD_ERR_UNSUPPORTED) continue;
+        if (s != TD_OK) return s;
+        if (cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
+          exec = nullptr;
+          cudaGetLastError();
+        } else {
+          g_loop_form_built.store(flat ? 2 : 1);
+        }
+        cudaGraphDestroy(g);
       }
-      td_status s = TD_OK;
-      if (cudaMemsetAsync(all_done, 0, sizeof(int), cs) != cudaSuccess ||
-          cudaMemsetAsync(w.loop, 0, sizeof(int), cs) != cudaSuccess)
-        s = TD_ERR_CUDA;
-      for (int t = t_start; t <= T && s == TD_OK; ++t)
-        s = run_step(dm, layers, ctx_len, nullptr, emb, pos, w_lm,
-                     phi_table + (size_t)(t - 1) * 6 * dm->d, t, T, gamma, rule, rope_theta,
-                     paging, precision, tokens, masked, conf, pred, n_committed, all_done, ws,
-                     cs, nsm, all_done, w.loop);
-      cudaGraph_t g = nullptr;
-      const cudaError_t ee = cudaStreamEndCapture(cs, &g);
-      if (s != TD_OK || ee != cudaSuccess || g == nullptr) {
-        if (g) cudaGraphDestroy(g);
-        cudaGetLastError();
-        return s != TD_OK ? s : TD_ERR_UNSUPPORTED;
-      }
-      const cudaError_t ie = cudaGraphInstantiate(&exec, g, 0);
-      cudaGraphDestroy(g);
-      if (ie != cudaSuccess) {
-        cudaGetLastError();
-        return TD_ERR_UNSUPPORTED;
-      }
+      if (exec == nullptr) return TD_ERR_UNSUPPORTED;
       g_loop_graphs[key] = exec;
       g_loop_order.push_back(key);
       if (g_loop_order.size() > kMaxLoopGraphs) {
@@ -972,6 +1094,11 @@ td_status td_timestep_table(const float* w_t, const float* b_t, int d, int T, fl
                           (cudaStream_t)stream>>>(w_t, b_t, rows, T, phi_table);
   TD_CUDA(cudaGetLastError());
   return TD_OK;
+}
+
+int td_decode_graph_form(int form) {
+  if (form == 1 || form == 2) g_loop_form_wanted.store(form);
+  return g_loop_form_built.load();
 }
 
 td_status td_check_bounded_wait(unsigned int limit_us, void* stream) {

@@ -299,10 +299,13 @@ __global__ void __launch_bounds__(1024)
                         int force_all, int rule, int* tokens, unsigned char* masked,
                         float* conf_out,
                         int* pred_out, int* n_committed, int* all_done, int* counters,
-                        const int* skip, int* steps_taken, const int* row_pos) {
+                        const int* skip, int* steps_taken, const int* row_pos,
+                        cudaGraphConditionalHandle next_step, int set_next_step) {
   // skip: the decode loop already finished; steps_taken (optional) counts the steps that ran;
   // row_pos (optional): the partials hold only the rows masked at the step start, row r at
-  // row_pos[r]; the other rows were not evaluated and get conf 0, pred -1
+  // row_pos[r]; the other rows were not evaluated and get conf 0, pred -1; with set_next_step
+  // (inside a decode-loop graph) the condition of the next step's node is set to "positions
+  // left"
   if (skip != nullptr && *skip != 0) return;
   if (steps_taken != nullptr && blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(steps_taken, 1);
   __shared__ float s_conf[64];
@@ -451,6 +454,7 @@ __global__ void __launch_bounds__(1024)
         __threadfence();
         const int left = atomicAdd(&counters[0], 0);
         *all_done = (left == 0) ? 1 : 0;
+        if (set_next_step) cudaGraphSetConditional(next_step, left != 0 ? 1u : 0u);
         counters[0] = 0;
         counters[1] = 0;
       }

@@ -262,10 +262,14 @@ td_status td_denoise_step(const td_dims* dims, const td_layer* layers, const int
  * (all [MASK] for a fresh block; a partially committed state resumes a stopped loop).
  * steps_taken: HOST int, set to the number of steps run.
  * Execution: the steps t_start..T are captured once per distinct argument set into a CUDA
- * graph (on a stream private to the library) and replayed on `stream`; every kernel of a step
- * returns at once when the previous step left nothing masked, so the call synchronises with
- * the host once per block (plus one read of `masked` on entry). If capture is not possible
- * the steps run from a host loop that reads all_done back after each step.
+ * graph (on a stream private to the library) and replayed on `stream`, so the call
+ * synchronises with the host once per block (plus one read of `masked` on entry). Each step
+ * sits in a conditional graph node whose condition the previous step's commit sets to
+ * "positions left": the steps after the one that committed the last position launch no
+ * kernel. Where conditional nodes are not available the graph is one flat capture whose
+ * kernels return at once when the previous step left nothing masked (see
+ * td_decode_graph_form). If capture is not possible the steps run from a host loop that reads
+ * all_done back after each step.
  * Returns TD_ERR_NOT_CONVERGED only if positions remain masked after step T (cannot
  * happen with force-commit at t == T; kept for callers that stop early). Alignment rules and
  * the other errors as in td_denoise_step (emb and pos are always read here). */
@@ -334,6 +338,13 @@ td_status td_device_error(int* code);
  * check that with td_device_error() (which also clears it) on its own GPU. No paper passage:
  * a property of this library. Asynchronous on stream. */
 td_status td_check_bounded_wait(unsigned int limit_us, void* stream);
+
+/* Diagnostic: the form of the decode-loop graphs (td_decode_block). form = 1 asks for the
+ * chain of conditional nodes (the default), form = 2 for the flat capture, for graphs built
+ * from now on in this process (each form is cached separately); any other value changes
+ * nothing. Returns the form of the last graph built in this process (0 before the first).
+ * No paper passage: a property of this library. No device work. */
+int td_decode_graph_form(int form);
 
 /* td_lmhead_commit without a caller-provided workspace. The pages have no counterpart: this
  * is a convenience of the library for callers that cannot allocate device memory, such as

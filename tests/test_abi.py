@@ -202,3 +202,10 @@ def test_unknown_attention_precision_is_rejected(lib):
     for bad in (2, -1):
         assert lib.td_block_attention(ctypes.byref(dm), fake, fake, fake, fake, fake, None, None,
                                       bad, fake, None, fake, 1 << 30, None) == 1
+
+
+def test_decode_graph_form_is_a_host_setting(lib):
+    # no graph has been built in this process: the form reads 0; unknown forms change nothing
+    assert lib.td_decode_graph_form(0) == 0
+    assert lib.td_decode_graph_form(7) == 0
+    assert lib.td_decode_graph_form(1) == 0

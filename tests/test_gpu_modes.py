@@ -175,6 +175,21 @@ def test_three_blocks_with_the_cache_growing_between_them(cuda_device):
         torch.cuda.synchronize()
         assert td.td_device_error() == 0 and not masked.any() and steps == t
         assert torch.equal(tokens, tk), blk
+        if blk == 0:
+            # the flat form of the loop graph (finished steps launch and return at once)
+            # decodes the same block in the same number of steps
+            assert td.td_decode_graph_form() == td.TD_GRAPH_CONDITIONAL
+            tf = torch.full_like(tokens, dm.V)
+            mf = torch.ones_like(masked)
+            td.td_decode_graph_form(td.TD_GRAPH_FLAT)
+            try:
+                steps_f = td.td_decode_block(dm.as_dict(), layers, emb, pos, w_lm, phi, dm.S,
+                                             0.8, tf, mf, ctx_len=ctx, ws=ws)
+                torch.cuda.synchronize()
+                assert td.td_decode_graph_form() == td.TD_GRAPH_FLAT
+            finally:
+                td.td_decode_graph_form(td.TD_GRAPH_CONDITIONAL)
+            assert steps_f == steps and torch.equal(tf, tokens) and not mf.any()
         # grow the caches with the committed block (the same tokens on both sides)
         tok = tokens.long()
         new = [(ktab[l][tok].contiguous(), vtab[l][tok].contiguous()) for l in range(dm.n_layers)]
