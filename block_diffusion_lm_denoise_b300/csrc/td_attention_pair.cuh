@@ -56,6 +56,82 @@ struct PairSmem {
   static constexpr int kBytes = kOffBar + 512 + 1024;
 };
 
+// The O readout at the end of a segment, out of line: it runs once per segment, and inline it
+// would sit in the per-tile loop's code.
+__device__ __noinline__ void pair_epilogue(uint16_t* out, float* part_o, float* part_ml, float* lse,
+                                           int S, int Hq, int R, uint32_t tmem, uint32_t lane_off,
+                                           int kh, int r, bool row_ok, float* xch, int bar_id,
+                                           uint64_t* o_done_bar, uint32_t parity,
+                                           uint64_t* o_free, bool even, int lane, float m_run,
+                                           float l_run, bool full, int b, int s_tok, int head,
+                                           size_t rec) {
+  constexpr int D = 128;
+  constexpr int DH = D / 2;
+  mbar_wait(o_done_bar, parity, ERR_WAIT_MMA);
+  tc_fence_after();
+  float* xl = xch + 512;
+  xl[kh * 128 + r] = l_run;
+  pair_sync(bar_id);
+  const float lo_other = xl[(1 - kh) * 128 + r];
+  const float ltot = kh == 0 ? l_run + lo_other : lo_other + l_run;
+  const float inv = 1.f / ltot;
+#pragma unroll 1
+  for (int k = 0; k < DH / 32; ++k) {
+    float o[32];
+    tmem_ld32(tmem + lane_off + kh * DH + 32 * k, o);
+    tmem_ld_wait();
+    if (!row_ok) continue;
+    if (full) {
+      uint4* d4 = reinterpret_cast<uint4*>(out +
+                                           (((size_t)b * S + s_tok) * Hq + head) * D + kh * DH +
+                                           32 * k);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        d4[j] = make_uint4(pack_bf16x2(o[8 * j] * inv, o[8 * j + 1] * inv),
+                           pack_bf16x2(o[8 * j + 2] * inv, o[8 * j + 3] * inv),
+                           pack_bf16x2(o[8 * j + 4] * inv, o[8 * j + 5] * inv),
+                           pack_bf16x2(o[8 * j + 6] * inv, o[8 * j + 7] * inv));
+    } else {
+      float4* d4 = reinterpret_cast<float4*>(part_o + (rec * R + r) * D + kh * DH + 32 * k);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        d4[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+    }
+  }
+  if (row_ok && kh == 0) {
+    if (full) {
+      if (lse)
+        lse[((size_t)b * S + s_tok) * Hq + head] = (m_run + __log2f(ltot)) * 0.6931471805599453f;
+    } else {
+      part_ml[(rec * R + r) * 2 + 0] = m_run;
+      part_ml[(rec * R + r) * 2 + 1] = ltot;
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    if (even) mbar_arrive(o_free);
+    else mbar_arrive_cluster_relaxed(cluster_addr(o_free, 0));
+  }
+}
+
+// Lazy rescale of this warp's O columns by alpha, out of line (rare).
+__device__ __noinline__ void pair_rescale(uint32_t tmem, uint32_t lane_off, int kh, float alpha,
+                                          uint64_t* o_done_bar, uint32_t parity) {
+  constexpr int DH = 64;
+  mbar_wait(o_done_bar, parity, ERR_WAIT_MMA);
+  tc_fence_after();
+#pragma unroll 1
+  for (int k = 0; k < DH / 8; ++k) {
+    uint32_t o[8];
+    tmem_ld8(tmem + lane_off + kh * DH + 8 * k, o);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+    tmem_st8(tmem + lane_off + kh * DH + 8 * k, o);
+  }
+}
+
 // kSplitP: P enters O += P V as two bf16 values, hi = bf16(P) over the first 64 columns of
 // SP[buf] and lo = bf16(P - hi) over the other 64 (both warps of a lane quarter have read
 // their scores by then), with a second product per key step: P is then carried to about
@@ -408,17 +484,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
           m_run = tmax;
           l_run *= alpha;
           // every PV so far (the last one used SP[(n-1) % 3]) must be done before O is touched
-          mbar_wait(&o_done[(n - 1) % kPairSP], ((n - 1) / kPairSP) & 1, ERR_WAIT_MMA);
-          tc_fence_after();
-#pragma unroll 1
-          for (int k = 0; k < DH / 8; ++k) {
-            uint32_t o[8];
-            tmem_ld8(tmem + lane_off + kh * DH + 8 * k, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st8(tmem + lane_off + kh * DH + 8 * k, o);
-          }
+          pair_rescale(tmem, lane_off, kh, alpha, &o_done[(n - 1) % kPairSP],
+                       ((n - 1) / kPairSP) & 1);
         }
         // P = 2^(x*scale - m) rounded to bf16, two per TMEM column (keys 64kh.. -> columns
         // 32kh.. of SP[buf]); the running sum adds the fp32 values
@@ -443,52 +510,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         hand_off(&p_full[buf]);
-        if (last) {
-          mbar_wait(&o_done[buf], (n / kPairSP) & 1, ERR_WAIT_MMA);
-          tc_fence_after();
-          // total row sum, added in the same order (half 0 + half 1) by both warps
-          float* xl = xch + 512;
-          xl[kh * 128 + r] = l_run;
-          pair_sync(bar_id);
-          const float lo_other = xl[(1 - kh) * 128 + r];
-          const float ltot = kh == 0 ? l_run + lo_other : lo_other + l_run;
-          const float inv = 1.f / ltot;
-#pragma unroll 1
-          for (int k = 0; k < DH / 32; ++k) {
-            float o[32];
-            tmem_ld32(tmem + lane_off + kh * DH + 32 * k, o);
-            tmem_ld_wait();
-            if (!row_ok) continue;
-            if (s.full) {
-              uint4* d4 = reinterpret_cast<uint4*>(
-                  p.out + (((size_t)s.b * p.S + s_tok) * p.Hq + head) * D + kh * DH + 32 * k);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                d4[j] = make_uint4(pack_bf16x2(o[8 * j] * inv, o[8 * j + 1] * inv),
-                                   pack_bf16x2(o[8 * j + 2] * inv, o[8 * j + 3] * inv),
-                                   pack_bf16x2(o[8 * j + 4] * inv, o[8 * j + 5] * inv),
-                                   pack_bf16x2(o[8 * j + 6] * inv, o[8 * j + 7] * inv));
-            } else {
-              float4* d4 =
-                  reinterpret_cast<float4*>(p.part_o + (rec * p.R + r) * D + kh * DH + 32 * k);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                d4[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-            }
-          }
-          if (row_ok && kh == 0) {
-            if (s.full) {
-              if (p.lse)
-                p.lse[((size_t)s.b * p.S + s_tok) * p.Hq + head] =
-                    (m_run + __log2f(ltot)) * 0.6931471805599453f;
-            } else {
-              p.part_ml[(rec * p.R + r) * 2 + 0] = m_run;
-              p.part_ml[(rec * p.R + r) * 2 + 1] = ltot;
-            }
-          }
-          tc_fence_before();
-          hand_off(o_free);
-        }
+        if (last)
+          pair_epilogue(p.out, p.part_o, p.part_ml, p.lse, p.S, p.Hq,
+                        p.R, tmem, lane_off, kh, r, row_ok, xch, bar_id, &o_done[buf],
+                        (n / kPairSP) & 1, o_free, even, lane, m_run, l_run, s.full, s.b, s_tok,
+                        head, rec);
         ++n;
         ++wi;
       }
