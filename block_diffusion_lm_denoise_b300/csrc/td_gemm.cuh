@@ -59,7 +59,8 @@ struct GemmSmem {
   static constexpr int kBBytes = BN * 128;       // BN rows x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes;
-  static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int kGateOffset = kBarOffset + 256;     // gate slices (EPI_RESID), 4 warps
+  static constexpr int kBytes = kGateOffset + 4 * BN * 4 + 1024;   // + alignment slack
 };
 
 // One epilogue thread's share of a finished tile: accumulator row `row` (of M live rows),
@@ -68,9 +69,18 @@ struct GemmSmem {
 template <int BN, int EPI>
 __device__ __forceinline__ bool gemm_epilogue(const GemmParams& p, int M, int row, int nt,
                                               uint32_t taddr, uint64_t* acc_full,
-                                              uint32_t parity) {
+                                              uint32_t parity, float* sgate) {
   const bool row_ok = row < M;
   if constexpr (EPI == EPI_RESID) {
+    // the tile's gate slice, the same for every row, staged by each epilogue warp in its own
+    // copy in shared memory while the MMAs run, so no chunk of the epilogue waits on a
+    // global load (a copy per warp: no barrier across warps, whose bounded waits may end
+    // differently)
+    const int lane = threadIdx.x & 31;
+    sgate += ((threadIdx.x >> 5) & 3) * BN;
+    __syncwarp();
+    for (int i = lane; i < BN; i += 32) sgate[i] = nt * BN + i < p.N ? p.gate[nt * BN + i] : 0.f;
+    __syncwarp();
     // The residual slice of this thread's row is loaded while the MMAs run, so the
     // epilogue waits on no global load once the accumulator is ready.
     const int out_row = !row_ok ? -1 : (p.row_pos != nullptr ? p.row_pos[row] : row);
@@ -84,7 +94,7 @@ __device__ __forceinline__ bool gemm_epilogue(const GemmParams& p, int M, int ro
     tc_fence_after();
     uint4* o4 = reinterpret_cast<uint4*>((p.row_pos != nullptr ? p.h_out : p.h) +
                                          (size_t)out_row * p.N + nt * BN);
-    const float4* g4 = reinterpret_cast<const float4*>(p.gate + nt * BN);
+    const float4* g4 = reinterpret_cast<const float4*>(sgate);
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
@@ -94,8 +104,8 @@ __device__ __forceinline__ bool gemm_epilogue(const GemmParams& p, int M, int ro
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint4 hv = hreg[4 * c + j];
-          const float4 ga = __ldg(&g4[8 * c + 2 * j]);
-          const float4 gb = __ldg(&g4[8 * c + 2 * j + 1]);
+          const float4 ga = g4[8 * c + 2 * j];
+          const float4 gb = g4[8 * c + 2 * j + 1];
           uint4 w;
           w.x = pack_bf16x2(bf16lo_to_f32(hv.x) + ga.x * v[8 * j + 0],
                             bf16hi_to_f32(hv.x) + ga.y * v[8 * j + 1]);
@@ -309,7 +319,8 @@ __global__ void __launch_bounds__(256, 1)
       const int acc = lt & 1;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       if (!gemm_epilogue<BN, EPI>(p, M, mt * 128 + q * 32 + lane, nt, taddr, &acc_full[acc],
-                                  (lt >> 1) & 1))
+                                  (lt >> 1) & 1,
+                                  reinterpret_cast<float*>(smem + L::kGateOffset)))
         break;
       tc_fence_before();
       mbar_arrive(&acc_empty[acc]);
@@ -343,7 +354,8 @@ struct GemmPairSmem {
   static constexpr int kBBytes = 128 * 128;      // this CTA's 128 rows of B x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes;
-  static constexpr int kBytes = kBarOffset + 256 + 1024;
+  static constexpr int kGateOffset = kBarOffset + 256;     // gate slices (EPI_RESID), 4 warps
+  static constexpr int kBytes = kGateOffset + 4 * 256 * 4 + 1024;
 };
 
 template <int STAGES, int EPI>
@@ -474,7 +486,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const int acc = lt & 1;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       if (!gemm_epilogue<BN, EPI>(p, M, mp * 256 + (int)rank * 128 + q * 32 + lane, nt, taddr,
-                                  &acc_full[acc], (lt >> 1) & 1))
+                                  &acc_full[acc], (lt >> 1) & 1,
+                                  reinterpret_cast<float*>(smem + L::kGateOffset)))
         break;
       // the accumulator is free once all four warps of both CTAs have read it
       tc_fence_before();
