@@ -600,56 +600,75 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // Log-sum-exp merge of the partials of every (unit, row chunk) that no single team covered.
-// Grid: (unit, chunk) x ceil(R / kMergeRows) row groups; thread (row, 4 columns).
+// Grid: (unit, chunk) x ceil(R / kMergeRows) row groups; thread (row, 4 columns). One thread
+// per CTA finds the teams that share the unit and their record indices (64-bit integer
+// arithmetic, done once instead of by every thread) and hands them over in shared memory.
 constexpr int kMergeRows = 16;
+constexpr int kMergeTeams = 16;   // teams per unit handled per pass of the record loop
+
+// The team whose key range holds (unit, tile) index x: the largest k with lo(k) <= x, i.e.
+// k * total < (x + 1) * n_teams.
+__device__ __forceinline__ int attn_owner(long long x, long long total, int n_teams) {
+  const long long k = ((x + 1) * n_teams - 1) / total;
+  return (int)(k < n_teams - 1 ? k : n_teams - 1);
+}
 
 __global__ void __launch_bounds__(512) attn_merge_kernel(const AttnParams p) {
   if (p.skip != nullptr && *p.skip != 0) return;
+  __shared__ int s_k[2];
+  __shared__ int s_rec[kMergeTeams];
   const int uc = blockIdx.x;
   const int unit = uc / p.NC;
   const int chunk = uc % p.NC;
-  const long long first_tile = (long long)unit * p.T;
-  const long long last_tile = first_tile + p.T - 1;
-  // team owning a tile x: the largest k with lo(k) <= x (lo is monotone in k)
-  auto owner = [&](long long x) {
-    int a = 0, b = p.n_teams - 1;
-    while (a < b) {
-      const int mid = (a + b + 1) >> 1;
-      if (attn_lo(mid, p.total, p.n_teams) <= x) a = mid; else b = mid - 1;
-    }
-    return a;
-  };
-  const int k0 = owner(first_tile);
-  const int k1 = owner(last_tile);
+  if (threadIdx.x == 0) {
+    const long long first_tile = (long long)unit * p.T;
+    s_k[0] = attn_owner(first_tile, p.total, p.n_teams);
+    s_k[1] = attn_owner(first_tile + p.T - 1, p.total, p.n_teams);
+  }
+  __syncthreads();
+  const int k0 = s_k[0];
+  const int k1 = s_k[1];
   if (k0 == k1) return;   // written directly by its only team
   const int b = unit / p.Hkv;
   const int g = unit % p.Hkv;
   const int D = p.D;
   const int nq4 = D / 4;
   const int r = blockIdx.y * kMergeRows + threadIdx.x / nq4;
-  if (threadIdx.x >= kMergeRows * nq4 || r >= p.R) return;
+  // threads past the rows stay for the barriers of the record loop
+  const bool row_ok = threadIdx.x < kMergeRows * nq4 && r < p.R;
   const int d4 = threadIdx.x % nq4;
-  // at most 4 teams share a unit in practice; larger spans loop
+  // the teams' records, kMergeTeams at a time; maximum first, then the weighted sums, both
+  // over the teams in order
   float M = -INFINITY;
-  for (int k = k0; k <= k1; ++k) {
-    const int rec = (k * p.NC + chunk) * p.max_seg +
-                    (unit - (int)(attn_lo(k, p.total, p.n_teams) / p.T));
-    M = fmaxf(M, __ldg(&p.part_ml[((size_t)rec * p.R + r) * 2]));
-  }
   float Lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = k0; k <= k1; ++k) {
-    const int rec = (k * p.NC + chunk) * p.max_seg +
-                    (unit - (int)(attn_lo(k, p.total, p.n_teams) / p.T));
-    const float mk = __ldg(&p.part_ml[((size_t)rec * p.R + r) * 2]);
-    const float lk = __ldg(&p.part_ml[((size_t)rec * p.R + r) * 2 + 1]);
-    if (lk == 0.f) continue;
-    const float w = exp2f(mk - M);
-    Lsum += lk * w;
-    const float4 o =
-        __ldg(reinterpret_cast<const float4*>(p.part_o + ((size_t)rec * p.R + r) * D) + d4);
-    acc.x += o.x * w; acc.y += o.y * w; acc.z += o.z * w; acc.w += o.w * w;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int kb = k0; kb <= k1; kb += kMergeTeams) {
+      const int nk = min(kMergeTeams, k1 - kb + 1);
+      __syncthreads();
+      if (threadIdx.x < nk)
+        s_rec[threadIdx.x] =
+            ((kb + threadIdx.x) * p.NC + chunk) * p.max_seg +
+            (unit - (int)(attn_lo(kb + threadIdx.x, p.total, p.n_teams) / p.T));
+      __syncthreads();
+      if (!row_ok) continue;
+      for (int i = 0; i < nk; ++i) {
+        const size_t rr = (size_t)s_rec[i] * p.R + r;
+        const float mk = __ldg(&p.part_ml[rr * 2]);
+        if (pass == 0) {
+          M = fmaxf(M, mk);
+          continue;
+        }
+        const float lk = __ldg(&p.part_ml[rr * 2 + 1]);
+        if (lk == 0.f) continue;
+        const float w = exp2f(mk - M);
+        Lsum += lk * w;
+        const float4 o = __ldg(reinterpret_cast<const float4*>(p.part_o + rr * D) + d4);
+        acc.x += o.x * w; acc.y += o.y * w; acc.z += o.z * w; acc.w += o.w * w;
+      }
+    }
   }
+  if (!row_ok) return;
   const float inv = 1.f / Lsum;
   const int s_tok = r / p.Gc;
   const int head = g * p.G + chunk * p.Gc + (r % p.Gc);
