@@ -405,7 +405,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
     const bool row_ok = chunk_ok && r < p.R;
     const int bar_id = 1 + q4;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    constexpr int DH = D / 2;
     // hand-off to the even CTA's gating barriers: a local release arrive there, a relaxed
     // arrive through the cluster window from the odd CTA (each follows a completed
     // tcgen05.wait::ld / ::st and tcgen05.fence::before_thread_sync)
