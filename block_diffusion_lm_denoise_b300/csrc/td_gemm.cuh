@@ -90,34 +90,81 @@ __device__ __forceinline__ bool gemm_epilogue(const GemmParams& p, int M, int ro
 #pragma unroll
     for (int j = 0; j < BN / 8; ++j)
       hreg[j] = (live && nt * BN + 8 * j < p.N) ? h4[j] : make_uint4(0, 0, 0, 0);
+    // each lane octet stores its eight rows through a transpose, one row's 128 bytes a store
+    int orow[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) orow[j] = __shfl_sync(0xffffffffu, out_row, (lane & ~7) + j);
+    uint16_t* dst = p.row_pos != nullptr ? p.h_out : p.h;
     if (!mbar_wait(acc_full, parity, ERR_WAIT_MMA)) return false;
     tc_fence_after();
-    uint4* o4 = reinterpret_cast<uint4*>((p.row_pos != nullptr ? p.h_out : p.h) +
-                                         (size_t)out_row * p.N + nt * BN);
     const float4* g4 = reinterpret_cast<const float4*>(sgate);
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      tmem_ld32(taddr + c * 32, v);
+    for (int c = 0; c < BN / 64; ++c) {
+      float v[64];
+      tmem_ld32(taddr + c * 64, *reinterpret_cast<float (*)[32]>(&v[0]));
+      tmem_ld32(taddr + c * 64 + 32, *reinterpret_cast<float (*)[32]>(&v[32]));
       tmem_ld_wait();
-      if (live && nt * BN + c * 32 < p.N) {
+      uint4 w[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 hv = hreg[4 * c + j];
-          const float4 ga = g4[8 * c + 2 * j];
-          const float4 gb = g4[8 * c + 2 * j + 1];
-          uint4 w;
-          w.x = pack_bf16x2(bf16lo_to_f32(hv.x) + ga.x * v[8 * j + 0],
-                            bf16hi_to_f32(hv.x) + ga.y * v[8 * j + 1]);
-          w.y = pack_bf16x2(bf16lo_to_f32(hv.y) + ga.z * v[8 * j + 2],
-                            bf16hi_to_f32(hv.y) + ga.w * v[8 * j + 3]);
-          w.z = pack_bf16x2(bf16lo_to_f32(hv.z) + gb.x * v[8 * j + 4],
-                            bf16hi_to_f32(hv.z) + gb.y * v[8 * j + 5]);
-          w.w = pack_bf16x2(bf16lo_to_f32(hv.w) + gb.z * v[8 * j + 6],
-                            bf16hi_to_f32(hv.w) + gb.w * v[8 * j + 7]);
-          o4[4 * c + j] = w;
-        }
+      for (int j = 0; j < 8; ++j) {
+        const uint4 hv = hreg[8 * c + j];
+        const float4 ga = g4[16 * c + 2 * j];
+        const float4 gb = g4[16 * c + 2 * j + 1];
+        w[j].x = pack_bf16x2(bf16lo_to_f32(hv.x) + ga.x * v[8 * j + 0],
+                             bf16hi_to_f32(hv.x) + ga.y * v[8 * j + 1]);
+        w[j].y = pack_bf16x2(bf16lo_to_f32(hv.y) + ga.z * v[8 * j + 2],
+                             bf16hi_to_f32(hv.y) + ga.w * v[8 * j + 3]);
+        w[j].z = pack_bf16x2(bf16lo_to_f32(hv.z) + gb.x * v[8 * j + 4],
+                             bf16hi_to_f32(hv.z) + gb.y * v[8 * j + 5]);
+        w[j].w = pack_bf16x2(bf16lo_to_f32(hv.w) + gb.z * v[8 * j + 6],
+                             bf16hi_to_f32(hv.w) + gb.w * v[8 * j + 7]);
       }
+      octet_transpose(w, lane & 7);
+      const int col = nt * BN + 64 * c + 8 * (lane & 7);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (orow[j] >= 0 && col + 8 <= p.N)
+          *reinterpret_cast<uint4*>(dst + (size_t)orow[j] * p.N + col) = w[j];
+    }
+    return true;
+  }
+  if constexpr (EPI == EPI_QKV) {
+    // 64-column chunks (q, k and v each start on a multiple of 64 columns), stored through
+    // the octet transpose like the residual epilogue
+    const int lane = threadIdx.x & 31;
+    if (!mbar_wait(acc_full, parity, ERR_WAIT_MMA)) return false;
+    tc_fence_after();
+    const int rb = row - (lane & 7);   // the octet's first row
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      float v[64];
+      tmem_ld32(taddr + c * 64, *reinterpret_cast<float (*)[32]>(&v[0]));
+      tmem_ld32(taddr + c * 64 + 32, *reinterpret_cast<float (*)[32]>(&v[32]));
+      tmem_ld_wait();
+      uint4 w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        w[j] = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]),
+                          pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                          pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                          pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+      octet_transpose(w, lane & 7);
+      const int col0 = nt * BN + 64 * c;
+      if (col0 >= p.N) continue;
+      uint16_t* base;
+      int width, cl;
+      if (col0 < p.nq) {
+        base = p.q; width = p.nq; cl = col0;
+      } else if (col0 < p.nq + p.nk) {
+        base = p.k; width = p.nk; cl = col0 - p.nq;
+      } else {
+        base = p.v; width = p.nk; cl = col0 - p.nq - p.nk;
+      }
+      cl += 8 * (lane & 7);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (rb + j < M)
+          *reinterpret_cast<uint4*>(base + (size_t)(rb + j) * width + cl) = w[j];
     }
     return true;
   }
@@ -153,8 +200,8 @@ __device__ __forceinline__ bool gemm_epilogue(const GemmParams& p, int M, int ro
 #pragma unroll
       for (int j = 0; j < 32; ++j) s += ex2_approx((v[j] - run_max) * 1.4426950408889634f);
       run_sum += s;
-    } else if constexpr (EPI == EPI_QKV || EPI == EPI_QKV_ROPE) {
-      if (EPI == EPI_QKV_ROPE && row_ok && col0 < p.N && col0 < p.nq + p.nk) {
+    } else if constexpr (EPI == EPI_QKV_ROPE) {
+      if (row_ok && col0 < p.N && col0 < p.nq + p.nk) {
         // the 32 columns of a chunk lie in one head (head_dim is 64 or 128)
         const int hd0 = (col0 < p.nq ? col0 : col0 - p.nq) % p.head_dim;
         const float2* cs = p.rope_cs + (size_t)row * (p.head_dim / 2) + hd0 / 2;

@@ -465,6 +465,29 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // max(a, b, c) in one instruction
+// 8 x 8 transpose of 16-byte elements within each octet of lanes (lanes 8g .. 8g + 7): on
+// entry lane 8g + i holds row i of its octet's matrix in x[0..7], on exit column i, i.e.
+// x[j] = element i of lane 8g + j's row. Three butterfly stages; in the stage of distance s a
+// lane swaps the four elements whose index differs from its own lane index in bit s with the
+// partner lane (index ^ s), which puts them at index ^ s. All 32 lanes take part.
+__device__ __forceinline__ void octet_transpose(uint4 (&x)[8], int lane) {
+#pragma unroll
+  for (int s = 4; s >= 1; s >>= 1) {
+    const bool hi = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i & s) continue;
+      uint4 v = hi ? x[i] : x[i + s];
+      v.x = __shfl_xor_sync(0xffffffffu, v.x, s);
+      v.y = __shfl_xor_sync(0xffffffffu, v.y, s);
+      v.z = __shfl_xor_sync(0xffffffffu, v.z, s);
+      v.w = __shfl_xor_sync(0xffffffffu, v.w, s);
+      if (hi) x[i] = v;
+      else x[i + s] = v;
+    }
+  }
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
