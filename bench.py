@@ -48,18 +48,52 @@ PROFILES = os.path.join(ROOT, "profiles")
 CSRC = os.path.join(ROOT, "block_diffusion_lm_denoise_b300", "csrc")
 
 
+def code_text(src: str) -> str:
+    """C/C++/CUDA source with its comments removed and every run of white space turned into
+    one space, so that an edit of comments or layout alone keeps a source's hash (string and
+    character literals are kept as they are)."""
+    out = []
+    i, n = 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def source_hash(sources) -> str:
+    """sha1 over the code text (see code_text) of the given kernel sources, in order."""
+    import hashlib
+    h = hashlib.sha1()
+    for f in sources:
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            h.update(code_text(fh.read()).encode())
+        h.update(b"\0")
+    return h.hexdigest()
+
+
 def traffic_per_launch(kernel: str, sources, units: int):
     """DRAM bytes (read + write) per launch of `kernel` from the ncu summaries committed under
     profiles/ ("traffic-record:" lines), scaled from the captured case to `units` (traffic
     grows in proportion to the units processed). None when no record matches the current
-    sources (the kernel changed since its counters were taken)."""
+    sources (the kernel's code changed since its counters were taken; comments do not
+    count)."""
     import glob
-    import hashlib
-    h = hashlib.sha1()
-    for f in sources:
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(fh.read())
-    sha = h.hexdigest()
+    sha = source_hash(sources)
     for path in sorted(glob.glob(os.path.join(PROFILES, "*.md"))):
         with open(path) as fh:
             for line in fh:

@@ -1,5 +1,5 @@
 // td_gemm.cuh -- persistent tcgen05 GEMM  C[M, N] = A[M, K] * B[N, K]^T  (bf16 in, fp32
-// accumulate in TMEM) with three fused epilogues:
+// accumulate in TMEM) with four fused epilogues:
 //   EPI_QKV    : bf16 store of the [q | k | v] projection into three row-major tensors
 //   EPI_QKV_ROPE: the same with q and k rotated first (rotary positional variant)
 //   EPI_RESID  : gated residual  h[r, n] = bf16(h[r, n] + gate[n] * C[r, n])  (in place, or
@@ -16,6 +16,9 @@
 // a narrow window of B tiles (the weights) and every weight byte leaves HBM about once.
 // gemm_pair_kernel (below) runs the same epilogues on 256 x 256 tiles over SM pairs; the
 // library uses it for every 256-wide GEMM and this kernel with BN = 128 for few rows.
+// The QKV and residual epilogues store 64-column chunks through an 8 x 8 transpose within
+// each lane octet, so that one store instruction writes whole 128-byte rows; the residual
+// epilogue reads the gate slice from a per-warp copy in shared memory.
 #pragma once
 
 #include "td_ptx.cuh"

@@ -33,8 +33,8 @@ def test_traffic_record_matches_the_source_hash_and_scales_by_units(tmp_path, mo
     (src / "b.cuh").write_text("kernel source two\n")
     import hashlib
     h = hashlib.sha1()
-    h.update(b"kernel source one\n")
-    h.update(b"kernel source two\n")
+    h.update(b"kernel source one\0")
+    h.update(b"kernel source two\0")
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "k.md").write_text(
@@ -44,8 +44,16 @@ def test_traffic_record_matches_the_source_hash_and_scales_by_units(tmp_path, mo
     monkeypatch.setattr(bench, "CSRC", str(src))
     monkeypatch.setattr(bench, "PROFILES", str(prof))
     assert bench.traffic_per_launch("my_kernel", ["a.cuh", "b.cuh"], 25) == 2500
-    # a changed source (or another order of the hashed files) finds no record: null traffic
+    # another order of the hashed files finds no record: null traffic
     assert bench.traffic_per_launch("my_kernel", ["b.cuh", "a.cuh"], 25) is None
+    # comments and layout do not count, code does
+    (src / "a.cuh").write_text("// a note\nkernel   source /* inline */ one\n")
+    assert bench.traffic_per_launch("my_kernel", ["a.cuh", "b.cuh"], 25) == 2500
     (src / "a.cuh").write_text("kernel source one, edited\n")
     assert bench.traffic_per_launch("my_kernel", ["a.cuh", "b.cuh"], 25) is None
+
+
+def test_code_text_keeps_literals_and_drops_comments():
+    src = 'asm("a // b"); /* c */ int x = 1; // d\nchar q = \'/\';'
+    assert bench.code_text(src) == 'asm("a // b"); int x = 1; char q = \'/\';'
 
