@@ -107,6 +107,48 @@ def test_decode_block_left_to_right_takes_s_steps_in_order(cuda_device):
         assert np.array_equal(got[:, t], tok_ref[:, t]), t
 
 
+@pytest.mark.parametrize("form", [td.TD_GRAPH_CONDITIONAL, td.TD_GRAPH_FLAT])
+def test_decode_block_resumes_a_stopped_loop(cuda_device, form):
+    # a block decoded for three steps through td_denoise_step and then handed to the loop at
+    # t_start = 4 ends exactly like the loop run from step 1 (the graph built for t_start = 4
+    # holds steps 4..T only); a block with nothing masked takes no step
+    dm = synth.Dims(B=3, S=16, d=256, Hq=8, Hkv=2, D=128, V=1024, Lmax=64, n_layers=2)
+    layers, w_lm, emb, pos, phi = _small_model(47, dm, cuda_device, w_scale=0.08)
+    ctx = torch.tensor([64, 20, 0], dtype=torch.int32, device=cuda_device)
+    ws = td.workspace(dm.as_dict(), td.TD_FN_DECODE_BLOCK, cuda_device)
+
+    def fresh():
+        return (torch.full((dm.B, dm.S), dm.V, dtype=torch.int32, device=cuda_device),
+                torch.ones((dm.B, dm.S), dtype=torch.uint8, device=cuda_device))
+
+    td.td_decode_graph_form(form)
+    try:
+        tf, mf = fresh()
+        steps_full = td.td_decode_block(dm.as_dict(), layers, emb, pos, w_lm, phi, dm.S, 0.8,
+                                        tf, mf, ctx_len=ctx, ws=ws)
+        torch.cuda.synchronize()
+        assert td.td_device_error() == 0 and not mf.any()
+        assert steps_full > 3, steps_full
+        tp, mp = fresh()
+        for t in range(1, 4):
+            td.td_denoise_step(dm.as_dict(), layers, w_lm, phi[t - 1], t, dm.S, 0.8, tp, mp,
+                               emb=emb, pos=pos, ctx_len=ctx, ws=ws)
+        steps_rest = td.td_decode_block(dm.as_dict(), layers, emb, pos, w_lm, phi, dm.S, 0.8,
+                                        tp, mp, t_start=4, ctx_len=ctx, ws=ws)
+        torch.cuda.synchronize()
+        assert td.td_device_error() == 0 and not mp.any()
+        assert td.td_decode_graph_form() == form
+        assert steps_rest == steps_full - 3
+        assert torch.equal(tp, tf)
+        # nothing masked on entry: no step runs and the block is left as it is
+        steps_none = td.td_decode_block(dm.as_dict(), layers, emb, pos, w_lm, phi, dm.S, 0.8,
+                                        tp, mp, ctx_len=ctx, ws=ws)
+        torch.cuda.synchronize()
+        assert steps_none == 0 and torch.equal(tp, tf)
+    finally:
+        td.td_decode_graph_form(td.TD_GRAPH_CONDITIONAL)
+
+
 def test_kv_append_matches_oracle_and_flags_overflow(cuda_device):
     B, S, Hkv, D, Lmax, n_layers = 3, 16, 2, 128, 70, 2
     dm = td.make_dims(B=B, S=S, d=256, Hq=8, Hkv=Hkv, D=D, V=64, Lmax=Lmax, n_layers=n_layers)
