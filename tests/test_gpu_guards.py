@@ -51,6 +51,9 @@ SHAPES = [
     (3, 16, 32, 2, 128, 383, [383, 0, 129]),   # SM pairs, three tiles, empty and ragged
     (2, 64, 8, 2, 128, 200, [200, 63]),        # the largest block, S = 64
     (1, 48, 32, 2, 128, 129, None),            # S = 48: 96-row chunks on SM pairs
+    (37, 16, 8, 2, 64, 100, None),             # B*S = 592: the GEMMs on SM pairs with a
+                                               # ragged last row pair, V = 1000: a ragged
+                                               # last vocabulary tile
 ]
 
 
@@ -127,3 +130,42 @@ def test_attention_lmhead_and_append_write_only_their_outputs(cuda_device):
     for g in (kc, vc, o, lse, aws, tok, msk, conf, pred, ncom, done, lws):
         assert g.intact()
     assert ctx2.cpu().tolist() == [300, 16, 116]
+
+
+def test_lmhead_on_sm_pairs_with_ragged_rows_and_vocabulary(cuda_device):
+    # 592 rows: the last 256-row pair tile holds 80 live rows; V = 1000: the last 256-column
+    # vocabulary tile holds 232 columns. Every written buffer is guarded; sampled rows in
+    # every row tile, the ragged one included, match the oracle.
+    import oracle
+    from parity_util import compare_commit
+    B, S, d, V = 37, 16, 512, 1000
+    M = B * S
+    dims = td.make_dims(B=B, S=S, d=d, Hq=8, Hkv=2, D=64, V=V, Lmax=0, n_layers=0)
+    h = synth.normal((M, d), 1.0, 13, "h", cuda_device)
+    w = synth.normal((V, d), 0.2, 13, "w", cuda_device)
+    t0 = torch.full((B, S), V, dtype=torch.int32)
+    tok = Guarded((B, S), torch.int32, cuda_device, t0)
+    msk = Guarded((B, S), torch.uint8, cuda_device, torch.ones((B, S), dtype=torch.uint8))
+    conf = Guarded((B, S), torch.float32, cuda_device)
+    pred = Guarded((B, S), torch.int32, cuda_device)
+    ncom = Guarded((B,), torch.int32, cuda_device)
+    done = Guarded((1,), torch.int32, cuda_device)
+    lws = Guarded((max(256, td.td_workspace_size(dims, td.TD_FN_LMHEAD_COMMIT)),), torch.uint8,
+                  cuda_device)
+    td.td_lmhead_commit(dims, h, w, 0.8, False, tok.t, msk.t, conf=conf.t, pred=pred.t,
+                        n_committed=ncom.t, all_done=done.t, ws=lws.t)
+    torch.cuda.synchronize()
+    assert td.td_device_error() == 0
+    for g in (tok, msk, conf, pred, ncom, done, lws):
+        assert g.intact()
+    seqs = [0, 15, 16, 31, 32, 36]          # rows 0.., 240.., 256.., 496.., 512.., 576..591
+    rows = [b * S + i for b in seqs for i in range(S)]
+    c_ref, p_ref, gap, _ = oracle.lmhead_confidence(h, w, rows=rows)
+    nb = len(seqs)
+    tok_ref, msk_ref, _, _ = oracle.commit(c_ref.reshape(nb, S), p_ref.reshape(nb, S),
+                                           t0[seqs].numpy(), np.ones((nb, S), bool), 0.8, False)
+    compare_commit(dict(conf=c_ref.reshape(nb, S), pred=p_ref.reshape(nb, S),
+                        gap=gap.reshape(nb, S), tokens=tok_ref, masked=msk_ref),
+                   dict(conf=conf.t[seqs].cpu().numpy(), pred=pred.t[seqs].cpu().numpy(),
+                        tokens=tok.t[seqs].cpu().numpy(), masked=msk.t[seqs].cpu().numpy()),
+                   np.ones((nb, S), bool), 0.8)
