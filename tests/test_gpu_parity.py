@@ -74,6 +74,8 @@ ATTN_CASES = [
     (2, 64, 32, 2, 128, 300, [300, 45]),      # the largest block, S = 64: 8 chunks per unit
     (2, 48, 32, 2, 128, 260, None),           # S = 48: 96-row chunks on SM pairs
     (1, 5, 8, 2, 64, 130, None),              # odd S: one 20-row chunk per KV head
+    (1, 16, 32, 2, 128, 8192, None),          # 2 units on 74 pairs: 37 teams per unit, so
+                                              # the merge reads its records in three passes
 ]
 
 
