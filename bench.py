@@ -529,7 +529,7 @@ def main():
     attn_traffic = traffic_per_launch(
         attn_kernel, ["td_ptx.cuh", "td_attention.cuh", "td_attention_pair.cuh"],
         dm.B * dm.Hkv * dm.Lmax)
-    lm_kernel = "gemm_pair_kernel<6,EPI_LMHEAD>"   # 256 x 256 tiles on SM pairs (M > 128)
+    lm_kernel = "gemm_pair_kernel<7,EPI_LMHEAD>"   # 256 x 256 tiles on SM pairs (M > 128)
     lm_traffic = traffic_per_launch(lm_kernel, ["td_ptx.cuh", "td_gemm.cuh"], M)
     roof_attn = {"kernel": attn_kernel, "bound": "hbm",
                  "achieved": round(attn_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",

@@ -396,23 +396,25 @@ __global__ void __launch_bounds__(256, 1)
 // `acc_full` barriers; the epilogue warps of both CTAs arrive (one arrive per warp) on the
 // even CTA's `acc_empty`.
 // ------------------------------------------------------------------------------------------
-constexpr int kPairGemmStages = 6;
+// Ring depth: seven 32 KB stages where the shared memory allows, six for the residual
+// epilogue, which also keeps the gate slices there.
+__host__ __device__ constexpr int pair_gemm_stages(int epi) { return epi == EPI_RESID ? 6 : 7; }
 
-template <int STAGES>
+template <int STAGES, int EPI>
 struct GemmPairSmem {
   static constexpr int kABytes = 128 * 128;      // this CTA's 128 rows of A x 64 bf16
   static constexpr int kBBytes = 128 * 128;      // this CTA's 128 rows of B x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarOffset = STAGES * kStageBytes;
   static constexpr int kGateOffset = kBarOffset + 256;     // gate slices (EPI_RESID), 4 warps
-  static constexpr int kBytes = kGateOffset + 4 * 256 * 4 + 1024;
+  static constexpr int kBytes = kGateOffset + (EPI == EPI_RESID ? 4 * 256 * 4 : 0) + 1024;
 };
 
 template <int STAGES, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-  using L = GemmPairSmem<STAGES>;
+  using L = GemmPairSmem<STAGES, EPI>;
   constexpr int BN = 256;
   if (p.skip != nullptr && *p.skip != 0) return;   // both CTAs of a pair read the same flag
   extern __shared__ uint8_t smem_raw[];

@@ -243,7 +243,7 @@ td_status launch_gemm(const void* A, const void* Bm, int M, int N, int K, GemmPa
 template <int STAGES, int EPI>
 td_status launch_gemm_pair(const void* A, const void* Bm, int M, int N, int K, GemmParams gp,
                            cudaStream_t st, int nsm) {
-  using L = GemmPairSmem<STAGES>;
+  using L = GemmPairSmem<STAGES, EPI>;
   CUtensorMap ma, mb;
   const uint64_t da[2] = {(uint64_t)K, (uint64_t)M}, sa[1] = {(uint64_t)K * 2};
   const uint64_t db[2] = {(uint64_t)K, (uint64_t)N}, sb[1] = {(uint64_t)K * 2};
@@ -268,7 +268,7 @@ template <int EPI>
 td_status gemm_dispatch(const void* A, const void* Bm, int M, int N, int K, GemmParams gp,
                         cudaStream_t st, int nsm, int bn) {
   if (bn == 128) return launch_gemm<128, 6, EPI>(A, Bm, M, N, K, gp, st, nsm);
-  return launch_gemm_pair<kPairGemmStages, EPI>(A, Bm, M, N, K, gp, st, nsm);
+  return launch_gemm_pair<pair_gemm_stages(EPI), EPI>(A, Bm, M, N, K, gp, st, nsm);
 }
 
 // adaLN-single modulation: the column-slab path for d = 256 * k (d <= 8192) with 16-byte
@@ -594,11 +594,12 @@ void set_all_smem() {
   set_smem(gemm_tn_kernel<128, 6, EPI_RESID>, GemmSmem<128, 6>::kBytes);
   set_smem(gemm_tn_kernel<128, 6, EPI_LMHEAD>, GemmSmem<128, 6>::kBytes);
   set_smem(gemm_tn_kernel<128, 6, EPI_QKV_ROPE>, GemmSmem<128, 6>::kBytes);
-  using GP = GemmPairSmem<kPairGemmStages>;
-  set_smem(gemm_pair_kernel<kPairGemmStages, EPI_QKV>, GP::kBytes);
-  set_smem(gemm_pair_kernel<kPairGemmStages, EPI_RESID>, GP::kBytes);
-  set_smem(gemm_pair_kernel<kPairGemmStages, EPI_LMHEAD>, GP::kBytes);
-  set_smem(gemm_pair_kernel<kPairGemmStages, EPI_QKV_ROPE>, GP::kBytes);
+  constexpr int sq = pair_gemm_stages(EPI_QKV), sr = pair_gemm_stages(EPI_RESID);
+  constexpr int sl = pair_gemm_stages(EPI_LMHEAD), sp = pair_gemm_stages(EPI_QKV_ROPE);
+  set_smem(gemm_pair_kernel<sq, EPI_QKV>, GemmPairSmem<sq, EPI_QKV>::kBytes);
+  set_smem(gemm_pair_kernel<sr, EPI_RESID>, GemmPairSmem<sr, EPI_RESID>::kBytes);
+  set_smem(gemm_pair_kernel<sl, EPI_LMHEAD>, GemmPairSmem<sl, EPI_LMHEAD>::kBytes);
+  set_smem(gemm_pair_kernel<sp, EPI_QKV_ROPE>, GemmPairSmem<sp, EPI_QKV_ROPE>::kBytes);
   set_smem(attn_fused_kernel<128, false, false>, AttnSmem<128>::kBytes);
   set_smem(attn_fused_kernel<64, false, false>, AttnSmem<64>::kBytes);
   set_smem(attn_pair_kernel<false, false>, PairSmem::kBytes);
