@@ -40,7 +40,6 @@ namespace td {
 constexpr int kPairKSlots = 5;      // K ring: 16 KB slots (64 keys x 128 dims)
 constexpr int kPairVSlots = 6;      // V ring: 16 KB slots (128 keys x 64 dims)
 constexpr int kPairSP = 3;          // score / probability buffers in TMEM
-constexpr int kPairPrefetch = 4;    // L2 prefetch distance of the producers, in tiles
 
 struct PairSmem {
   static constexpr int kKHalf = 64 * 128;                     // 64 keys x 64 dims
@@ -239,18 +238,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
       for (int u = u_first; u <= u_last && ok; ++u) {
         const SegInfo s = attn_seg(p, lo, hi, u);
         if (attn_seg_work(p, s) == 0) continue;
-        const int ctx_end = s.t1 < s.nvt ? s.t1 : s.nvt;
-        // this CTA's half of context tile t: K rows 64r.. (both dim halves), V dims 64r..
-        auto prefetch = [&](int t) {
-          int y, z;
-          if (!attn_ctx_coords<kPaged>(p, s.b, s.g, t, y, z)) return;
-          if (is_v) tma_prefetch_l2_3d(mc, kx, y, z);
-          else
-            for (int kh = 0; kh < 2; ++kh) tma_prefetch_l2_3d(mc, kh * 64, y + ky, z);
-        };
         bool q_pending = !is_v;
         if (q_pending && sg == 0) {
-          // the first Q goes out before the ring fills and prefetches queue up behind it
+          // the first Q goes out before the ring fills
           q_pending = false;
           if (even) mbar_arrive_expect_tx(q_full, q_bytes);
           for (int kh = 0; kh < 2; ++kh)
@@ -258,10 +248,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttnThreads, 1)
                              s.g * p.G + chunk * p.Gc, 0, s.b);
           ++sg;
         }
-        for (int t = s.t0; t < s.t0 + kPairPrefetch && t < ctx_end; ++t) prefetch(t);
         for (int t = s.t0; t < s.t1; ++t) {
           if (!attn_tile_live(p, s, t)) continue;
-          if (t + kPairPrefetch < ctx_end) prefetch(t + kPairPrefetch);
           const int st = n % nslot;
           if (n >= nslot && !mbar_wait(&empty[st], ((n / nslot) & 1) ^ 1, ERR_WAIT_MMA)) {
             ok = false;
