@@ -61,7 +61,6 @@ struct AttnParams {
 
 constexpr int kKSlots = 3;         // K ring (a slot is freed when S of its tile is done)
 constexpr int kVSlots = 4;         // V ring (a slot is freed when PV of its tile is done)
-constexpr int kPrefetch = 4;       // L2 prefetch distance of the producers, in tiles
 constexpr int kAttnThreads = 384;   // 8 softmax warps + 2 producers + 2 MMA issuers
 constexpr int kKProducerWarp = 8;
 constexpr int kVProducerWarp = 9;
@@ -288,18 +287,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int u = u_first; u <= u_last && ok; ++u) {
         const SegInfo s = attn_seg(p, lo, hi, u);
         if (attn_seg_work(p, s) == 0) continue;
-        const int ctx_end = s.t1 < s.nvt ? s.t1 : s.nvt;     // live context tiles end here
-        // L2 prefetch kPrefetch tiles ahead of the ring loads, so that a ring load mostly
-        // hits L2 and its slot turns over in less time
-        auto prefetch = [&](int t) {
-          int y, z;
-          if (attn_ctx_coords<kPaged>(p, s.b, s.g, t, y, z))
-            for (int kh = 0; kh < D / 64; ++kh) tma_prefetch_l2_3d(mc, kh * 64, y, z);
-        };
-        for (int t = s.t0; t < s.t0 + kPrefetch && t < ctx_end; ++t) prefetch(t);
         for (int t = s.t0; t < s.t1; ++t) {
           if (!attn_tile_live(p, s, t)) continue;
-          if (t + kPrefetch < ctx_end) prefetch(t + kPrefetch);
           const int st = n % nslot;
           if (n >= nslot && !mbar_wait(&empty[st], ((n / nslot) & 1) ^ 1, ERR_WAIT_MMA)) {
             ok = false;
